@@ -1,0 +1,322 @@
+"""Seeded synthetic inputs for paged-KV decode.
+
+This module only draws random numbers and lays them out in the paged cache
+format; it holds none of the attention or metadata arithmetic.  Both the CUDA
+path (through the ctypes binding) and the CPU oracle consume exactly the bytes
+produced here.
+
+Cache layouts are the vLLM ones restated on the page "paged_attention_v2_triton.py"
+(kernel argument comments of ``_paged_attn_v2_partition_kernel``):
+
+* ``query``        ``[num_seqs, num_heads, head_size]``
+* ``key_cache``    ``[num_blocks, num_kv_heads, head_size // x, block_size, x]``
+  with ``x = 16 // element_size``
+* ``value_cache``  ``[num_blocks, num_kv_heads, head_size, block_size]``
+* ``block_tables`` ``[num_seqs, max_blocks_per_seq]`` int32 (may be a strided view)
+* ``seq_lens``     ``[num_seqs]`` int32
+
+Named workloads (``WORKLOADS``) reproduce the five decode batches this library
+is measured on; each is described by what it is and its sizes.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+__all__ = [
+    "DTYPES",
+    "WorkloadSpec",
+    "WORKLOADS",
+    "make_inputs",
+    "make_workload",
+    "x_pack",
+]
+
+DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+# Sentinels written into block-table entries that no sequence owns.  Any kernel
+# that reads one would see an out-of-range block id.
+UNUSED_ENTRY = -1
+GAP_ENTRY = -7  # columns skipped by a strided (column-step) view
+
+
+def x_pack(dtype: torch.dtype) -> int:
+    """Elements per 16-byte group of the key cache's innermost dimension."""
+    return 16 // torch.empty((), dtype=dtype).element_size()
+
+
+@dataclass
+class WorkloadSpec:
+    """Shape and value recipe of one synthetic decode batch."""
+
+    name: str
+    description: str
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    block_size: int
+    dtype: str
+    seq_len_recipe: str  # "fixed", "uniform", "lognormal"
+    seq_lens: Optional[List[int]] = None  # for "fixed"
+    seq_len_lo: int = 1
+    seq_len_hi: int = 1
+    lognormal_median: float = 1024.0
+    lognormal_sigma: float = 1.0
+    num_blocks: Optional[int] = None  # None -> ceil(1.1 * blocks needed)
+    first_row: Optional[List[int]] = None  # fixed block-table row for seq 0
+    bt_col_step: int = 1  # >1: table allocated wider and read as [:, ::step]
+    max_blocks_per_seq: Optional[int] = None  # None -> cdiv(max seq_len, block_size)
+    peaky_fraction: float = 0.0  # fraction of (token, kv_head) key vectors scaled
+    peaky_scale: float = 8.0
+    mode: str = "v1"  # "v1", "v2_fixed", "v2_splits"
+    partition_size: int = 512
+    max_kv_splits: int = 16
+    device_core_count: int = 148
+    extra: Dict = field(default_factory=dict)
+
+
+WORKLOADS: Dict[str, WorkloadSpec] = {
+    "tiny_mha_fp32": WorkloadSpec(
+        name="tiny_mha_fp32",
+        description=("tiny MHA decode, fp32: 2 seqs, seq_lens {16, 13}, 4 heads = 4 kv heads, "
+                     "head_size 64, block_size 8, 64 blocks; seq 0 block table [40, 30]"),
+        num_seqs=2, num_heads=4, num_kv_heads=4, head_size=64, block_size=8, dtype="f32",
+        seq_len_recipe="fixed", seq_lens=[16, 13], num_blocks=64, first_row=[40, 30],
+        mode="v1",
+    ),
+    "mha_v1_fp16": WorkloadSpec(
+        name="mha_v1_fp16",
+        description=("MHA single-pass decode, fp16: 64 seqs, 32 heads = 32 kv heads, head_size 128, "
+                     "block_size 16, seq_lens uniform in [512, 4096]"),
+        num_seqs=64, num_heads=32, num_kv_heads=32, head_size=128, block_size=16, dtype="f16",
+        seq_len_recipe="uniform", seq_len_lo=512, seq_len_hi=4096, mode="v1",
+    ),
+    "gqa_v1_bf16": WorkloadSpec(
+        name="gqa_v1_bf16",
+        description=("GQA single-pass decode, bf16: 256 seqs, 32 query heads / 8 kv heads, "
+                     "head_size 128, block_size 16, seq_lens uniform in [128, 2048]"),
+        num_seqs=256, num_heads=32, num_kv_heads=8, head_size=128, block_size=16, dtype="bf16",
+        seq_len_recipe="uniform", seq_len_lo=128, seq_len_hi=2048, mode="v1",
+    ),
+    "long_v2_bf16": WorkloadSpec(
+        name="long_v2_bf16",
+        description=("long-context split-KV decode, bf16: 8 seqs of 16k..128k tokens, 64 query heads / "
+                     "8 kv heads, head_size 128, block_size 16, partition 512, 1% of keys x8"),
+        num_seqs=8, num_heads=64, num_kv_heads=8, head_size=128, block_size=16, dtype="bf16",
+        seq_len_recipe="fixed",
+        seq_lens=[k * 1024 for k in (16, 24, 32, 48, 64, 96, 112, 128)],
+        peaky_fraction=0.01, peaky_scale=8.0, mode="v2_fixed", partition_size=512,
+    ),
+    "ragged_v2_bf16": WorkloadSpec(
+        name="ragged_v2_bf16",
+        description=("ragged serving batch + metadata, bf16: 512 seqs, log-normal seq_lens "
+                     "(median 1024, sigma 1, clipped to [1, 32768]), 32 query heads / 8 kv heads, "
+                     "head_size 128, block_size 16; int32 table [512, 2048] read as a stride-2 "
+                     "column view; page_indices copy, num_kv_splits (max 16, 148 SMs), split-KV"),
+        num_seqs=512, num_heads=32, num_kv_heads=8, head_size=128, block_size=16, dtype="bf16",
+        seq_len_recipe="lognormal", lognormal_median=1024.0, lognormal_sigma=1.0,
+        seq_len_lo=1, seq_len_hi=32768, bt_col_step=2, max_blocks_per_seq=2048,
+        mode="v2_splits", max_kv_splits=16, device_core_count=148,
+    ),
+}
+
+
+def _gen(seed: int, stream: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1009 + stream)
+    return g
+
+
+def _draw_seq_lens(spec: WorkloadSpec, seed: int) -> List[int]:
+    g = _gen(seed, 1, "cpu")
+    if spec.seq_len_recipe == "fixed":
+        return list(spec.seq_lens)
+    if spec.seq_len_recipe == "uniform":
+        t = torch.randint(spec.seq_len_lo, spec.seq_len_hi + 1, (spec.num_seqs,), generator=g)
+        return [int(v) for v in t]
+    if spec.seq_len_recipe == "lognormal":
+        z = torch.randn(spec.num_seqs, generator=g, dtype=torch.float64)
+        raw = torch.exp(math.log(spec.lognormal_median) + spec.lognormal_sigma * z)
+        lens = torch.clamp(torch.round(raw), spec.seq_len_lo, spec.seq_len_hi)
+        return [int(v) for v in lens]
+    raise ValueError(spec.seq_len_recipe)
+
+
+def make_inputs(
+    *,
+    num_heads: int,
+    num_kv_heads: int,
+    head_size: int,
+    block_size: int,
+    dtype: str,
+    seq_lens: Sequence[int],
+    num_blocks: Optional[int] = None,
+    first_row: Optional[Sequence[int]] = None,
+    bt_col_step: int = 1,
+    max_blocks_per_seq: Optional[int] = None,
+    peaky_fraction: float = 0.0,
+    peaky_scale: float = 8.0,
+    unused_slot_fill: Optional[float] = None,
+    seed: int = 0,
+    device="cpu",
+) -> Dict:
+    """Draw one paged decode batch.
+
+    * query, key_cache and value_cache entries are N(0, 1) drawn in float32 and
+      rounded once to ``dtype``.
+    * Every sequence gets ``cdiv(seq_len, block_size)`` distinct physical
+      blocks; no block is shared between sequences.  Block ids are a seeded
+      random permutation of ``range(num_blocks)``, except that ``first_row``
+      (when given) pins sequence 0's blocks and the others avoid them.
+    * ``peaky_fraction``: each (block, slot, kv_head) key vector is multiplied
+      by ``peaky_scale`` when a seeded uniform draw is below the fraction
+      (applied in float32, before rounding to ``dtype``).
+    * ``unused_slot_fill``: when set, cache slots that no sequence owns (and
+      the tail slots of each sequence's last block) are overwritten with this
+      value, e.g. NaN, to check that kernels never let them reach a result.
+    * The block table is allocated ``[num_seqs, max_blocks_per_seq * bt_col_step]``
+      and returned as the column view ``[:, ::bt_col_step]``; entries that no
+      sequence owns hold -1, skipped columns hold -7.
+
+    Random draws happen on ``device`` (a CUDA generator when it is a GPU) so
+    multi-GB batches need no host-side generation; small batches default to
+    the CPU.  Returned tensors live on ``device``.
+    """
+    dt = DTYPES[dtype]
+    x = x_pack(dt)
+    seq_lens = [int(v) for v in seq_lens]
+    B = len(seq_lens)
+    if head_size % x:
+        raise ValueError("head_size must be a multiple of x")
+    nblk = [(L + block_size - 1) // block_size for L in seq_lens]
+    needed = sum(nblk)
+    if num_blocks is None:
+        num_blocks = max(1, math.ceil(1.1 * needed))
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = max([1] + nblk)
+    if max(nblk + [0]) > max_blocks_per_seq:
+        raise ValueError("a sequence needs more blocks than max_blocks_per_seq")
+
+    # --- block tables (host side: small) ---
+    g_tab = _gen(seed, 2, "cpu")
+    perm = torch.randperm(num_blocks, generator=g_tab).tolist()
+    rows: List[List[int]] = []
+    if first_row is not None:
+        if len(first_row) != nblk[0]:
+            raise ValueError("first_row length must equal cdiv(seq_lens[0], block_size)")
+        pinned = set(int(b) for b in first_row)
+        pool = [b for b in perm if b not in pinned]
+        rows.append([int(b) for b in first_row])
+        start = 1
+    else:
+        pool = perm
+        start = 0
+    if needed - (nblk[0] if first_row is not None else 0) > len(pool):
+        raise ValueError("num_blocks too small")
+    off = 0
+    for s in range(start, B):
+        rows.append(pool[off:off + nblk[s]])
+        off += nblk[s]
+    full = torch.full((B, max_blocks_per_seq * bt_col_step), GAP_ENTRY, dtype=torch.int32)
+    view = full[:, ::bt_col_step]
+    view.fill_(UNUSED_ENTRY)
+    for s in range(B):
+        if nblk[s]:
+            view[s, : nblk[s]] = torch.tensor(rows[s], dtype=torch.int32)
+    full = full.to(device)
+    block_tables = full[:, ::bt_col_step]
+
+    # --- dense tensors, drawn on the target device ---
+    Hk, D = num_kv_heads, head_size
+    g_q = _gen(seed, 3, device)
+    g_k = _gen(seed, 4, device)
+    g_v = _gen(seed, 5, device)
+    query = torch.randn((B, num_heads, D), generator=g_q, device=device, dtype=torch.float32).to(dt)
+    key_cache = torch.empty((num_blocks, Hk, D // x, block_size, x), dtype=dt, device=device)
+    value_cache = torch.empty((num_blocks, Hk, D, block_size), dtype=dt, device=device)
+    # Draw block by block in slabs to bound float32 temporaries.
+    slab = max(1, (1 << 26) // (Hk * D * block_size))
+    g_p = _gen(seed, 6, device)
+    for b0 in range(0, num_blocks, slab):
+        b1 = min(num_blocks, b0 + slab)
+        kk = torch.randn((b1 - b0, Hk, D // x, block_size, x), generator=g_k, device=device,
+                         dtype=torch.float32)
+        if peaky_fraction > 0.0:
+            u = torch.rand((b1 - b0, Hk, 1, block_size, 1), generator=g_p, device=device,
+                           dtype=torch.float32)
+            kk = torch.where(u < peaky_fraction, kk * peaky_scale, kk)
+        key_cache[b0:b1] = kk.to(dt)
+        vv = torch.randn((b1 - b0, Hk, D, block_size), generator=g_v, device=device,
+                         dtype=torch.float32)
+        value_cache[b0:b1] = vv.to(dt)
+        del kk, vv
+
+    if unused_slot_fill is not None:
+        owned = torch.zeros((num_blocks, block_size), dtype=torch.bool)
+        for s in range(B):
+            for j, b in enumerate(rows[s]):
+                n = min(block_size, seq_lens[s] - j * block_size)
+                owned[b, :n] = True
+        owned = owned.to(device)
+        kmask = (~owned).view(num_blocks, 1, 1, block_size, 1).expand_as(key_cache)
+        vmask = (~owned).view(num_blocks, 1, 1, block_size).expand_as(value_cache)
+        key_cache[kmask] = unused_slot_fill
+        value_cache[vmask] = unused_slot_fill
+
+    seq_lens_t = torch.tensor(seq_lens, dtype=torch.int32, device=device)
+    return {
+        "query": query,
+        "key_cache": key_cache,
+        "value_cache": value_cache,
+        "block_tables": block_tables,
+        "block_tables_storage": full,
+        "seq_lens": seq_lens_t,
+        "seq_lens_list": seq_lens,
+        "block_rows": rows,
+        "num_blocks": num_blocks,
+        "num_heads": num_heads,
+        "num_kv_heads": num_kv_heads,
+        "head_size": D,
+        "block_size": block_size,
+        "x": x,
+        "dtype": dtype,
+        "scale": 1.0 / math.sqrt(D),
+        "max_blocks_per_seq": max_blocks_per_seq,
+    }
+
+
+def make_workload(name: str, seed: int = 0, device="cpu", **overrides) -> Dict:
+    """Inputs of a named workload; ``overrides`` replace spec fields (e.g. ``num_seqs``)."""
+    spec = WORKLOADS[name]
+    if overrides:
+        spec = WorkloadSpec(**{**spec.__dict__, **overrides})
+    lens = _draw_seq_lens(spec, seed)[: spec.num_seqs]
+    inp = make_inputs(
+        num_heads=spec.num_heads,
+        num_kv_heads=spec.num_kv_heads,
+        head_size=spec.head_size,
+        block_size=spec.block_size,
+        dtype=spec.dtype,
+        seq_lens=lens,
+        num_blocks=spec.num_blocks,
+        first_row=spec.first_row,
+        bt_col_step=spec.bt_col_step,
+        max_blocks_per_seq=spec.max_blocks_per_seq,
+        peaky_fraction=spec.peaky_fraction,
+        peaky_scale=spec.peaky_scale,
+        seed=seed,
+        device=device,
+    )
+    # cu_num_blocks: the indptr a serving engine hands to the page-index copy
+    # (exclusive scan of each sequence's block count).
+    nblk = [len(r) for r in inp["block_rows"]]
+    cu = [0]
+    for n in nblk:
+        cu.append(cu[-1] + n)
+    inp["cu_num_blocks"] = torch.tensor(cu, dtype=torch.int32, device=device)
+    inp["spec"] = spec
+    return inp
