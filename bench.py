@@ -1,0 +1,592 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV decode hot path on one GB300 (or N replicas).
+
+One *step* is one pass of the whole decode path over one synthetic batch:
+for the ragged serving batch (the default workload) that is
+
+    copy_page_indices -> compute_num_kv_splits -> paged_attention_v2_partition
+    (reading block ids through the flat page list) -> paged_attention_v2_reduce
+
+all launched through the C ABI on one stream.  The KV cache is resident
+device state (as in serving); inputs are larger than L2, so no flush is
+needed between steps (the tiny workload, which fits in L2, is flushed).
+
+Printed (rank 0, one JSON line): the KV-read GB/s of the step (``value``),
+microseconds per step, the roofline of the dominant kernel (the attention
+partition pass) against the measured HBM copy bandwidth, the end-to-end
+figure through host buffers, SM clocks sampled during the timed region and a
+CPU baseline: the float64 oracle timed on a bounded sample on the host cores.
+
+``--impl reference`` times that oracle alone as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode µs/step and KV-read GB/s (% of GB300 HBM peak) at 1 GPU"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "ragged_v2_bf16"
+
+
+# ----------------------------------------------------------------- helpers --
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_tables_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from a committed ncu
+    summary, only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_sha") == kernel_source_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------- the decode step --
+
+class DecodeStep:
+    """Device buffers of one workload and the launches of one step, issued
+    straight through the C ABI with argument structs prepared once."""
+
+    def __init__(self, name: str, seed: int, device):
+        import ctypes
+
+        import paged_kv_decode_tables_gb300 as pkv
+
+        self.pkv = pkv
+        self.lib = pkv.lib()
+        self.name = name
+        inp = workloads.make_workload(name, seed=seed, device=device)
+        self.inp = inp
+        spec = inp["spec"]
+        self.spec = spec
+        q, kc, vc = inp["query"], inp["key_cache"], inp["value_cache"]
+        B, H, D = q.shape
+        Hk, bs = kc.shape[1], kc.shape[3]
+        self.B, self.H, self.D, self.Hk, self.bs = B, H, D, Hk, bs
+        lens = inp["seq_lens_list"]
+        self.lens = lens
+        e = q.element_size()
+        nblk = [len(r) for r in inp["block_rows"]]
+        self.kv_bytes = sum(lens) * Hk * 2 * D * e
+        self.q_bytes = B * H * D * e
+        self.out_bytes = B * H * D * e
+        self.table_bytes = 4 * sum(nblk)
+        self.mode = spec.mode
+        dev = q.device
+        self.out = torch.empty_like(q)
+        c_i64x3 = ctypes.c_int64 * 3
+        self.out_stride = c_i64x3(*self.out.stride())
+        stream = 0  # replaced per call by the current stream
+        self._stream = stream
+
+        if self.mode == "v2_splits":
+            self.cu = inp["cu_num_blocks"]
+            self.page_indices = torch.empty(int(self.cu[-1].item()), dtype=torch.int32, device=dev)
+            self.splits = torch.empty(B, dtype=torch.int32, device=dev)
+            self.maxP = spec.max_kv_splits
+            bt_for_attn, indptr = self.page_indices, self.cu
+        else:
+            bt_for_attn, indptr = inp["block_tables"], None
+            if self.mode == "v2_fixed":
+                self.maxP = -(-inp["max_blocks_per_seq"] * bs // spec.partition_size)
+            else:
+                self.maxP = 1
+        if self.mode != "v1":
+            self.tmp = torch.empty(B, H, self.maxP, D, dtype=torch.float32, device=dev)
+            self.es = torch.empty(B, H, self.maxP, dtype=torch.float32, device=dev)
+            self.ml = torch.empty(B, H, self.maxP, dtype=torch.float32, device=dev)
+            self.partial_bytes = 0
+        self.args = pkv._decode_args(q, kc, vc, bt_for_attn, inp["seq_lens"], inp["scale"], indptr,
+                                     None, None)
+        self.args_ref = ctypes.byref(self.args)
+        self.launches_per_step = {"v1": 1, "v2_fixed": 2, "v2_splits": 4}[self.mode]
+        # Algorithmic bytes of one launch of the attention kernel: K+V of every
+        # token, the queries, the block ids and lengths it reads, and (single
+        # pass) its output.  The fp32 split-KV partials are counted apart.
+        self.attn_alg_bytes = (self.kv_bytes + self.q_bytes + self.table_bytes + 4 * B +
+                               (self.out_bytes if self.mode == "v1" else 0) +
+                               (4 * B + 4 * (B + 1) if self.mode == "v2_splits" else 0))
+
+    def _check(self, st, what):
+        if st != 0:
+            raise RuntimeError(f"{what} failed with status {st}")
+
+    def run(self, attn_events=None):
+        """Enqueue one step on the current stream; optionally record events
+        around the attention kernel."""
+        lib, pkv = self.lib, self.pkv
+        s = torch.cuda.current_stream().cuda_stream
+        if self.mode == "v2_splits":
+            inp = self.inp
+            bt = inp["block_tables"]
+            self._check(lib.copy_page_indices(self.page_indices.data_ptr(), self.page_indices.numel(),
+                                              bt.data_ptr(), bt.shape[1], bt.stride(0), bt.stride(1),
+                                              self.cu.data_ptr(), self.B, None, s), "copy")
+            sp = self.spec
+            self._check(lib.compute_num_kv_splits(self.splits.data_ptr(), inp["seq_lens"].data_ptr(),
+                                                  self.B, 1, self.H, self.Hk, sp.max_kv_splits,
+                                                  sp.device_core_count, s), "splits")
+        if attn_events is not None:
+            attn_events[0].record()
+        if self.mode == "v1":
+            self._check(lib.paged_attention_decode(self.out.data_ptr(), self.out_stride,
+                                                   self.args_ref, s), "decode")
+        else:
+            splits = self.splits.data_ptr() if self.mode == "v2_splits" else None
+            P = 0 if self.mode == "v2_splits" else self.spec.partition_size
+            self._check(lib.paged_attention_v2_partition(self.tmp.data_ptr(), self.es.data_ptr(),
+                                                         self.ml.data_ptr(), self.maxP, P, splits,
+                                                         self.args_ref, s), "partition")
+        if attn_events is not None:
+            attn_events[1].record()
+        if self.mode != "v1":
+            splits = self.splits.data_ptr() if self.mode == "v2_splits" else None
+            self._check(lib.paged_attention_v2_reduce(
+                self.out.data_ptr(), self.out_stride, self.tmp.data_ptr(), self.es.data_ptr(),
+                self.ml.data_ptr(), self.inp["seq_lens"].data_ptr(), splits, self.B, self.H,
+                self.D, self.bs, self.maxP, self.spec.partition_size, self.args.dtype, None, s),
+                "reduce")
+
+    def host_inputs(self):
+        """Pinned host copies of the per-step inputs (query, lengths, table,
+        indptr) and a pinned host buffer for the result."""
+        inp = self.inp
+        hin = {"query": inp["query"].cpu().pin_memory(),
+               "seq_lens": inp["seq_lens"].cpu().pin_memory(),
+               "table": inp["block_tables_storage"].cpu().pin_memory()}
+        if self.mode == "v2_splits":
+            hin["cu"] = self.cu.cpu().pin_memory()
+        hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        return hin, hout
+
+    def e2e_step(self, hin, hout):
+        inp = self.inp
+        inp["query"].copy_(hin["query"], non_blocking=True)
+        inp["seq_lens"].copy_(hin["seq_lens"], non_blocking=True)
+        inp["block_tables_storage"].copy_(hin["table"], non_blocking=True)
+        if "cu" in hin:
+            self.cu.copy_(hin["cu"], non_blocking=True)
+        self.run()
+        hout.copy_(self.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def e2e_bytes(self, hin, hout):
+        h2d = sum(t.numel() * t.element_size() for t in hin.values())
+        return h2d, hout.numel() * hout.element_size()
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample_inputs(step_or_inp, seq_ids):
+    """CPU copies of the pages of ``seq_ids`` (renumbered 0..n-1: the oracle's
+    result does not depend on physical block ids)."""
+    inp = step_or_inp
+    rows = [inp["block_rows"][s] for s in seq_ids]
+    blocks = [b for r in rows for b in r]
+    idx = torch.tensor(blocks, dtype=torch.long, device=inp["key_cache"].device)
+    kc = inp["key_cache"].index_select(0, idx).cpu() if blocks else inp["key_cache"][:0].cpu()
+    vc = inp["value_cache"].index_select(0, idx).cpu() if blocks else inp["value_cache"][:0].cpu()
+    width = max([1] + [len(r) for r in rows])
+    bt = torch.full((len(seq_ids), width), -1, dtype=torch.int32)
+    off = 0
+    for i, r in enumerate(rows):
+        bt[i, :len(r)] = torch.arange(off, off + len(r), dtype=torch.int32)
+        off += len(r)
+    q = inp["query"][torch.tensor(seq_ids, device=inp["query"].device)].cpu()
+    lens = [inp["seq_lens_list"][s] for s in seq_ids]
+    return q, kc, vc, bt, lens
+
+
+def oracle_step(inp, spec, seq_ids, all_splits):
+    """The oracle's pass over the sampled sequences (the same steps as the
+    GPU step: metadata, then split-KV partition + reduce or single pass)."""
+    import oracle
+
+    q, kc, vc, bt, lens = oracle_sample_inputs(inp, seq_ids)
+    if spec.mode == "v1":
+        oracle.decode_v1(q, kc, vc, bt, lens, inp["scale"])
+    elif spec.mode == "v2_fixed":
+        maxP = -(-max(lens) // spec.partition_size)
+        tmp, es, ml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], maxP,
+                                          partition_size=spec.partition_size)
+        oracle.v2_reduce(tmp, es, ml, lens, spec.block_size, partition_size=spec.partition_size)
+    else:
+        splits = [all_splits[s] for s in seq_ids]
+        tmp, es, ml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], spec.max_kv_splits,
+                                          num_kv_splits=splits)
+        oracle.v2_reduce(tmp, es, ml, lens, spec.block_size, num_kv_splits=splits)
+    e = inp["query"].element_size()
+    return sum(lens) * spec.num_kv_heads * 2 * spec.head_size * e
+
+
+def cpu_threads():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    torch.set_num_threads(n)
+    return torch.get_num_threads()
+
+
+def oracle_metadata(inp, spec):
+    import oracle
+
+    splits = None
+    if spec.mode == "v2_splits":
+        bt = inp["block_tables"].cpu()
+        cu = inp["cu_num_blocks"].cpu().tolist()
+        oracle.copy_page_indices(bt, cu, cu[-1])
+        splits = oracle.num_kv_splits(inp["seq_lens_list"], 1, spec.num_heads, spec.num_kv_heads,
+                                      spec.max_kv_splits, spec.device_core_count)
+    return splits
+
+
+def cpu_baseline(inp, spec, budget_s=10.0):
+    """The oracle on a bounded sample: sequences in a seeded order until the
+    time budget is spent; returns KV-read GB/s over the sample."""
+    cores = cpu_threads()
+    order = torch.randperm(len(inp["seq_lens_list"]), generator=torch.Generator().manual_seed(0))
+    t0 = time.perf_counter()
+    splits = oracle_metadata(inp, spec)
+    done, nbytes = [], 0
+    for s in order.tolist():
+        nbytes += oracle_step(inp, spec, [s], splits)
+        done.append(s)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{len(done)} of {len(inp['seq_lens_list'])} sequences "
+                       f"({nbytes / 1e9:.3f} GB of K/V) of {spec.name} plus the whole batch's "
+                       f"metadata, float64, {dt:.1f} s")}
+
+
+# ------------------------------------------------------------------ arms --
+
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return 0
+    spec = workloads.WORKLOADS[args.workload]
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = workloads.make_workload(args.workload, seed=0, device=device)
+    cores = cpu_threads()
+    total_budget = args.reference_budget
+    per_step = max(0.5, total_budget / max(1, args.steps + args.warmup))
+    order = torch.randperm(len(inp["seq_lens_list"]), generator=torch.Generator().manual_seed(0))
+    order = order.tolist()
+    pos = 0
+    splits = oracle_metadata(inp, spec)
+
+    def one_step():
+        nonlocal pos
+        t0 = time.perf_counter()
+        nb, n = 0, 0
+        while True:
+            nb += oracle_step(inp, spec, [order[pos % len(order)]], splits)
+            pos += 1
+            n += 1
+            if time.perf_counter() - t0 >= per_step:
+                break
+        return nb, time.perf_counter() - t0, n
+
+    for _ in range(args.warmup):
+        one_step()
+    tot_b, tot_t, tot_n = 0, 0.0, 0
+    for _ in range(args.steps):
+        b, t, n = one_step()
+        tot_b += b
+        tot_t += t
+        tot_n += n
+    value = tot_b / tot_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "description": spec.description},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                         "kind": "oracle",
+                         "sample": (f"each step: sequences of {args.workload} in a seeded order "
+                                    f"for ~{per_step:.1f} s ({tot_n} sequences over "
+                                    f"{args.steps} steps), float64")},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    rank, world, local_rank = env_rank()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU for the library arm")
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist = dist_mod
+
+    from paged_kv_decode_tables_gb300 import _build
+
+    if rank == 0 or dist is None:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    step = DecodeStep(args.workload, seed=rank, device="cuda")
+    spec = step.spec
+    flush = step.kv_bytes < 4 * L2_BYTES
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda") if flush else None
+
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device()) if (rank == 0 and not args.no_clocks) else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    if flush:
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(K)]
+        for i in range(K):
+            flush_buf.fill_(float(i))
+            step_ev[i][0].record()
+            step.run(attn_ev[i])
+            step_ev[i][1].record()
+        torch.cuda.synchronize()
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    else:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record()
+        for i in range(K):
+            step.run(attn_ev[i])
+        t_end.record()
+        torch.cuda.synchronize()
+        elapsed_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end to end through host buffers (per step: H2D of the inputs, the step,
+    # D2H of the output, host waits for it)
+    hin, hout = step.host_inputs()
+    Ke = max(3, min(K, 200))
+    for _ in range(3):
+        step.e2e_step(hin, hout)
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(Ke):
+        step.e2e_step(hin, hout)
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d, d2h = step.e2e_bytes(hin, hout)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    ms_step = elapsed_ms / K
+    value = world * step.kv_bytes / (ms_step * 1e-3) / 1e9
+    attn_sorted = sorted(attn_ms)
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    peak, peak_kind = load_peak()
+    achieved = step.attn_alg_bytes / (attn_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(step.inp, spec, budget_s=args.cpu_budget)
+    kern = {"v1": "paged_attention_decode", "v2_fixed": "paged_attention_v2_partition",
+            "v2_splits": "paged_attention_v2_partition"}[step.mode]
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if spec.dtype == "bf16" else spec.dtype,
+        "accumulate": "f32",
+        "data": "synthetic (seeded; see workloads.py)",
+        "config": {
+            "workload": args.workload,
+            "description": spec.description,
+            "num_seqs": step.B, "num_heads": step.H, "num_kv_heads": step.Hk,
+            "head_size": step.D, "block_size": step.bs,
+            "total_tokens": sum(step.lens), "kv_bytes_per_step": step.kv_bytes,
+            "l2": ("flushed between steps (512 MB write)" if flush else
+                   f"inputs larger than L2: {step.kv_bytes / 1e9:.2f} GB of K/V per step"),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "kernel": kern,
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} HBM copy bandwidth",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "alg_bytes_per_launch": step.attn_alg_bytes,
+            "avg_launch_us": round(attn_avg_ms * 1e3, 2),
+            "p10_p90_launch_us": [round(attn_sorted[len(attn_sorted) // 10] * 1e3, 2),
+                                  round(attn_sorted[(9 * len(attn_sorted)) // 10] * 1e3, 2)],
+        },
+        "step_share": {"attention_kernel": round(attn_avg_ms / ms_step, 4)},
+        "e2e": {"value": round(world * step.kv_bytes / (e2e_s / Ke) / 1e9, 2), "unit": UNIT,
+                "us_per_step": round(e2e_s / Ke * 1e6, 2), "steps": Ke,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "K/V cache resident on the device; per-step inputs from pinned host memory"},
+        "gpu_launches": K * step.launches_per_step,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--reference-budget", type=float, default=150.0,
+                    help="total seconds for --impl reference")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,248 @@
+/*
+ * paged_kv.h - C ABI of the GB300 (sm_103a) paged-KV decode library.
+ *
+ * Five operations make up the decode hot path:
+ *
+ *   paged_attention_decode        single-pass decode (one partition per sequence)
+ *   paged_attention_v2_partition  split-KV partition pass
+ *   paged_attention_v2_reduce     log-sum-exp combination of the partitions
+ *   copy_page_indices             block-table rows -> flat page list, through an indptr
+ *   compute_num_kv_splits         per-sequence split count
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - Every pointer argument is DEVICE memory owned and allocated by the caller.
+ *   The library never allocates, frees, copies to the host or synchronises; each
+ *   call enqueues its kernel(s) on `stream` and returns.  `stream == NULL` is the
+ *   legacy default stream.
+ * - Strides are in ELEMENTS (not bytes), int64.
+ * - Arguments are checked on the host before anything is launched; a rejected
+ *   call returns PKV_ERR_INVALID_ARG or PKV_ERR_UNSUPPORTED and enqueues nothing.
+ *   A launch failure reported by the CUDA runtime returns PKV_ERR_CUDA.
+ * - Device data the host cannot see (seq_lens, block ids, indptr entries, split
+ *   counts) is checked inside the kernels.  A bad value never faults or hangs:
+ *   the kernel clamps it, OR-s a PKV_ERRF_* bit into the optional `err_flag`
+ *   (a caller-zeroed device int32, may be NULL) and carries on; results that
+ *   depend on the bad value are then unspecified.
+ * - Arithmetic: fp32 accumulation for every input dtype; softmax statistics and
+ *   split-KV partials are fp32.
+ *
+ * Cache layouts (vLLM's, as restated on the page "paged_attention_v2_triton.py",
+ * argument comments of _paged_attn_v2_partition_kernel):
+ *   query        [num_seqs, num_heads, head_size]
+ *   key_cache    [num_blocks, num_kv_heads, head_size / x, block_size, x],  x = 16 / sizeof(elem)
+ *   value_cache  [num_blocks, num_kv_heads, head_size, block_size]
+ *   block_tables [num_seqs, max_blocks_per_seq] int32, any strides
+ * The (block, kv_head) page of each cache must be contiguous:
+ *   k_stride[2..4] == {block_size*x, x, 1} and v_stride[2..3] == {block_size, 1};
+ * the block and head strides are free (multiples of 16 bytes).
+ */
+#ifndef PAGED_KV_H
+#define PAGED_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent strides */
+  PKV_ERR_UNSUPPORTED = 2, /* valid but not built: head_size, block_size, group, layout */
+  PKV_ERR_CUDA = 3         /* the CUDA runtime refused the launch */
+} pkv_status_t;
+
+/* Bits OR-ed into *err_flag by kernels that meet bad device data. */
+#define PKV_ERRF_BLOCK_ID 1u /* block id outside [0, num_blocks): block 0 was read instead */
+#define PKV_ERRF_SEQ_LEN 2u  /* seq_len < 0 or above the row's capacity: clamped */
+#define PKV_ERRF_SPLITS 4u   /* num_kv_splits[s] outside [1, max_num_partitions]: clamped */
+#define PKV_ERRF_INDPTR 8u   /* indptr row negative, longer than the table, or past the output */
+#define PKV_ERRF_TIMEOUT 16u /* a wait for a copy into shared memory exceeded its time limit */
+
+/*
+ * Inputs shared by paged_attention_decode and paged_attention_v2_partition.
+ *
+ *   num_seqs, num_heads, num_kv_heads, head_size, block_size, x: shapes above;
+ *       num_heads % num_kv_heads == 0; query head h reads kv head
+ *       h / (num_heads / num_kv_heads) (contiguous groups).
+ *   max_blocks_per_seq: columns of block_tables; seq_len may not exceed
+ *       max_blocks_per_seq * block_size.
+ *   num_blocks: valid physical block ids are [0, num_blocks).
+ *   dtype: element type of query, key_cache, value_cache and the output.
+ *   scale: logit = scale * (q . k).
+ *   kv_indptr: optional.  NULL: sequence s's logical page j is
+ *       block_tables[s*bt_stride[0] + j*bt_stride[1]].  Non-NULL (num_seqs+1
+ *       int32): block_tables is a flat page list (e.g. the output of
+ *       copy_page_indices) and page j of sequence s is
+ *       block_tables[kv_indptr[s] + j*bt_stride[1]], with
+ *       kv_indptr[s+1]-kv_indptr[s] pages available to it.
+ *   seq_lens: [num_seqs] int32 context lengths.
+ *   err_flag: optional device int32 receiving PKV_ERRF_* bits.
+ */
+typedef struct {
+  int32_t num_seqs;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t head_size;
+  int32_t block_size;
+  int32_t x;
+  int32_t max_blocks_per_seq;
+  int32_t num_blocks;
+  pkv_dtype_t dtype;
+  float scale;
+  const void *query;
+  int64_t q_stride[3];
+  const void *key_cache;
+  int64_t k_stride[5];
+  const void *value_cache;
+  int64_t v_stride[4];
+  const int32_t *block_tables;
+  int64_t bt_stride[2];
+  const int32_t *kv_indptr;
+  const int32_t *seq_lens;
+  int32_t *err_flag;
+} pkv_decode_args_t;
+
+/* Library version string, e.g. "paged_kv 0.1.0 sm_103a". */
+const char *pkv_version(void);
+/* Static description of a status code. */
+const char *pkv_status_string(pkv_status_t status);
+/* sizeof(pkv_decode_args_t), for bindings that mirror the struct. */
+size_t pkv_decode_args_size(void);
+
+/*
+ * Tuning knob for paged_attention_decode / paged_attention_v2_partition: warps
+ * per CTA, i.e. how many warps split one (sequence, kv head, partition) unit.
+ * 0 (default) picks per call from the number of units and the SM count;
+ * 1 or 4 forces that value where the instance exists.  Process-wide.
+ * Returns PKV_ERR_INVALID_ARG for any other value.
+ */
+pkv_status_t pkv_set_attention_warps(int32_t warps);
+
+/*
+ * Single-pass paged decode.
+ *
+ * For every sequence s and query head h:
+ *   out[s, h, :] = sum_t softmax_t(scale * q[s,h] . k_t) * v_t   over t < seq_lens[s],
+ * where k_t / v_t are gathered through block = table[s, t / block_size],
+ * slot = t % block_size (page "Needs help on performance optimization",
+ * triton-lang/triton issue 2522, worked example; page
+ * "paged_attention_v2_triton.py", module docstring "Algorithm per instance").
+ * This is the split-KV computation with a single partition covering the whole
+ * sequence.
+ *
+ *   out: [num_seqs, num_heads, head_size] in args->dtype with strides out_stride.
+ *   A sequence with seq_len == 0 gets a zero output row.
+ * Supported: fp16/bf16 with head_size in {64, 128, 256}; fp32 with head_size in
+ * {64, 128}; block_size in {8, 16, 32}; num_heads/num_kv_heads <= 8.
+ */
+pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
+                                    const pkv_decode_args_t *args, pkv_stream_t stream);
+
+/*
+ * Split-KV partition pass (page "paged_attention_v2_triton.py",
+ * _paged_attn_v2_partition_kernel and "Algorithm per instance").
+ *
+ * Partition p of sequence s covers tokens [p*P, min((p+1)*P, seq_len)) where
+ *   P = partition_size                      when num_kv_splits == NULL, or
+ *   P = roundup(cdiv(seq_len, n), block_size), n = num_kv_splits[s], otherwise
+ *       (partitions p >= n are empty; this chunking is a reading: the split
+ *       heuristic only gives the count).
+ * For every (s, h, p) it writes, over the logits z of the partition's tokens:
+ *   max_logits[s,h,p] = max z                       (natural-log units)
+ *   exp_sums[s,h,p]   = sum exp(z - max z)
+ *   tmp_out[s,h,p,:]  = sum exp(z - max z) v / exp_sums[s,h,p]   (normalised)
+ * An empty partition (start >= seq_len, or p >= n) writes max_logits = -inf,
+ * exp_sums = 0 and leaves tmp_out untouched.
+ *
+ *   tmp_out:    [num_seqs, num_heads, max_num_partitions, head_size] fp32, contiguous.
+ *   exp_sums, max_logits: [num_seqs, num_heads, max_num_partitions] fp32, contiguous.
+ *   partition_size: multiple of block_size (ignored when num_kv_splits != NULL);
+ *       max_num_partitions >= cdiv(max_blocks_per_seq*block_size, partition_size).
+ *   num_kv_splits: optional [num_seqs] int32 (e.g. from compute_num_kv_splits).
+ * Same dtype/shape support as paged_attention_decode.
+ */
+pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float *max_logits,
+                                          int32_t max_num_partitions, int32_t partition_size,
+                                          const int32_t *num_kv_splits,
+                                          const pkv_decode_args_t *args, pkv_stream_t stream);
+
+/*
+ * Log-sum-exp reduce (page "paged_attention_v2_triton.py",
+ * _paged_attn_v2_reduce_kernel: global max, rescale, weighted sum).
+ *
+ * With num_parts the number of non-empty partitions of sequence s (computed
+ * from seq_lens and partition_size / num_kv_splits / block_size exactly as the
+ * partition pass does):
+ *   M = max_p max_logits[p],  w_p = exp(max_logits[p] - M) * exp_sums[p],
+ *   out[s,h,:] = sum_p w_p * tmp_out[s,h,p,:] / sum_p w_p     (p < num_parts).
+ * A sequence with seq_len == 0 gets a zero row.
+ *
+ *   out: [num_seqs, num_heads, head_size] in out_dtype with strides out_stride.
+ *   tmp_out / exp_sums / max_logits: as written by paged_attention_v2_partition.
+ *   head_size in {64, 128, 256}; max_num_partitions <= 4096.
+ */
+pkv_status_t paged_attention_v2_reduce(void *out, const int64_t out_stride[3],
+                                       const float *tmp_out, const float *exp_sums,
+                                       const float *max_logits, const int32_t *seq_lens,
+                                       const int32_t *num_kv_splits, int32_t num_seqs,
+                                       int32_t num_heads, int32_t head_size, int32_t block_size,
+                                       int32_t max_num_partitions, int32_t partition_size,
+                                       pkv_dtype_t out_dtype, int32_t *err_flag,
+                                       pkv_stream_t stream);
+
+/*
+ * Page-index copy (vLLM PR 35765, "AITER MLA backend: Avoid CPU sync in
+ * _build_decode", _copy_page_indices_kernel with the review's stride_1 change):
+ *   page_indices[cu_num_blocks[i] + j] = block_table[i*bt_stride0 + j*bt_stride1]
+ *   for 0 <= j < cu_num_blocks[i+1] - cu_num_blocks[i],  0 <= i < num_reqs.
+ * It replaces block_table[mask] (data-dependent size, hence a host sync) with a
+ * fixed-size launch.  Bit-exact.
+ *
+ *   page_indices: int32 output, page_indices_capacity entries; positions no row
+ *       covers are left untouched.  Writes past the capacity are skipped and flagged.
+ *   block_table: int32, num_cols columns per row, any strides.
+ *   cu_num_blocks: [num_reqs + 1] int32 indptr (non-decreasing).  A row longer
+ *       than num_cols is clamped and flagged (PKV_ERRF_INDPTR).
+ */
+pkv_status_t copy_page_indices(int32_t *page_indices, int64_t page_indices_capacity,
+                               const int32_t *block_table, int32_t num_cols, int64_t bt_stride0,
+                               int64_t bt_stride1, const int32_t *cu_num_blocks, int32_t num_reqs,
+                               int32_t *err_flag, pkv_stream_t stream);
+
+/*
+ * Per-sequence split count (sglang python/sglang/kernels/ops/attention/metadata.py,
+ * get_num_kv_splits_triton), one CTA, no host sync:
+ *   mx = max len, mn = min len (both over max(len, 1)); if mx*8 < mn*10: mn = mx
+ *   s1 = min(cdiv(mx, mn), max_kv_splits); c1 = cdiv(mx, s1)
+ *   ext = int32(float32(device_core_count) * max(log2_f32(float32(mx) / 64), 1))
+ *         (float32 product, log2 correctly rounded to float32, truncation)
+ *   G = num_head / num_kv_head
+ *   token_grid = num_seq*num_group*num_head                 if G == 1
+ *              = num_seq*num_group*cdiv(num_head, min(16, G)) otherwise
+ *   s2 = min(cdiv(ext, token_grid), max_kv_splits); c2 = cdiv(mx, s2)
+ *   num_kv_splits[s*num_group + i] = max(cdiv(len_s, c1), cdiv(len_s, c2)),  i < num_group
+ * Bit-exact.  A zero-length sequence gets 0.
+ *
+ *   num_kv_splits: [num_seq * num_group] int32 output.
+ *   seq_lens: [num_seq] int32.  num_seq >= 1, max_kv_splits >= 1,
+ *   device_core_count >= 1 (an argument, not queried).
+ */
+pkv_status_t compute_num_kv_splits(int32_t *num_kv_splits, const int32_t *seq_lens, int32_t num_seq,
+                                   int32_t num_group, int32_t num_head, int32_t num_kv_head,
+                                   int32_t max_kv_splits, int32_t device_core_count,
+                                   pkv_stream_t stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* PAGED_KV_H */

@@ -1,0 +1,303 @@
+"""Python binding of ``libpaged_kv.so`` (the C ABI in ``include/paged_kv.h``).
+
+Argument marshalling only: each function takes torch CUDA tensors, passes
+their device pointers, element strides and the current CUDA stream to the C
+entry point of the same name, and raises ``RuntimeError`` on a non-OK status.
+Every step of the decode path runs in the library's CUDA kernels; there is no
+fallback.  The library is loaded on first use and a missing build raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "PKV_ERRF_BLOCK_ID",
+    "PKV_ERRF_SEQ_LEN",
+    "PKV_ERRF_SPLITS",
+    "PKV_ERRF_INDPTR",
+    "PKV_ERRF_TIMEOUT",
+    "lib",
+    "lib_path",
+    "version",
+    "set_attention_warps",
+    "paged_attention_decode",
+    "paged_attention_v2_partition",
+    "paged_attention_v2_reduce",
+    "copy_page_indices",
+    "compute_num_kv_splits",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libpaged_kv.so")
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA = 0, 1, 2, 3
+PKV_ERRF_BLOCK_ID, PKV_ERRF_SEQ_LEN, PKV_ERRF_SPLITS, PKV_ERRF_INDPTR, PKV_ERRF_TIMEOUT = (
+    1, 2, 4, 8, 16)
+
+_DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+_c_i32, _c_i64, _c_f32, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+_I64x3 = _c_i64 * 3
+
+
+class DecodeArgs(ctypes.Structure):
+    """Mirror of ``pkv_decode_args_t``."""
+
+    _fields_ = [
+        ("num_seqs", _c_i32), ("num_heads", _c_i32), ("num_kv_heads", _c_i32),
+        ("head_size", _c_i32), ("block_size", _c_i32), ("x", _c_i32),
+        ("max_blocks_per_seq", _c_i32), ("num_blocks", _c_i32),
+        ("dtype", ctypes.c_int), ("scale", _c_f32),
+        ("query", _c_p), ("q_stride", _c_i64 * 3),
+        ("key_cache", _c_p), ("k_stride", _c_i64 * 5),
+        ("value_cache", _c_p), ("v_stride", _c_i64 * 4),
+        ("block_tables", _c_p), ("bt_stride", _c_i64 * 2),
+        ("kv_indptr", _c_p), ("seq_lens", _c_p), ("err_flag", _c_p),
+    ]
+
+
+_LIB = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with `python -m paged_kv_decode_tables_gb300._build` "
+            "(or __graft_entry__.build()); there is no fallback implementation")
+    L = ctypes.CDLL(_LIB_PATH)
+    L.pkv_version.restype = ctypes.c_char_p
+    L.pkv_version.argtypes = []
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_status_string.argtypes = [ctypes.c_int]
+    L.pkv_decode_args_size.restype = ctypes.c_size_t
+    L.pkv_decode_args_size.argtypes = []
+    L.pkv_set_attention_warps.restype = ctypes.c_int
+    L.pkv_set_attention_warps.argtypes = [_c_i32]
+    L.paged_attention_decode.restype = ctypes.c_int
+    L.paged_attention_decode.argtypes = [_c_p, ctypes.POINTER(_c_i64), ctypes.POINTER(DecodeArgs),
+                                         _c_p]
+    L.paged_attention_v2_partition.restype = ctypes.c_int
+    L.paged_attention_v2_partition.argtypes = [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_p,
+                                               ctypes.POINTER(DecodeArgs), _c_p]
+    L.paged_attention_v2_reduce.restype = ctypes.c_int
+    L.paged_attention_v2_reduce.argtypes = [_c_p, ctypes.POINTER(_c_i64), _c_p, _c_p, _c_p, _c_p,
+                                            _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                            ctypes.c_int, _c_p, _c_p]
+    L.copy_page_indices.restype = ctypes.c_int
+    L.copy_page_indices.argtypes = [_c_p, _c_i64, _c_p, _c_i32, _c_i64, _c_i64, _c_p, _c_i32,
+                                    _c_p, _c_p]
+    L.compute_num_kv_splits.restype = ctypes.c_int
+    L.compute_num_kv_splits.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                        _c_i32, _c_p]
+    if L.pkv_decode_args_size() != ctypes.sizeof(DecodeArgs):
+        raise RuntimeError("pkv_decode_args_t layout mismatch between the library and the binding")
+    _LIB = L
+    return L
+
+
+def version() -> str:
+    return lib().pkv_version().decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PKV_OK:
+        msg = lib().pkv_status_string(status).decode()
+        raise RuntimeError(f"{what} failed: {msg} (status {status})")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _cuda(t: Optional[torch.Tensor], name: str) -> None:
+    if t is not None and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library works on device memory)")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def set_attention_warps(warps: int) -> None:
+    """Force warps per CTA (1 or 4) for the attention kernels; 0 restores the default."""
+    _check(lib().pkv_set_attention_warps(int(warps)), "pkv_set_attention_warps")
+
+
+def _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
+                 err_flag, max_blocks_per_seq) -> DecodeArgs:
+    for t, n in ((query, "query"), (key_cache, "key_cache"), (value_cache, "value_cache"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens"),
+                 (kv_indptr, "kv_indptr"), (err_flag, "err_flag")):
+        _cuda(t, n)
+    if query.dtype not in _DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {query.dtype}")
+    if key_cache.dtype != query.dtype or value_cache.dtype != query.dtype:
+        raise ValueError("query, key_cache and value_cache must share a dtype")
+    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (kv_indptr, "kv_indptr"),
+                 (err_flag, "err_flag")):
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    if query.dim() != 3 or key_cache.dim() != 5 or value_cache.dim() != 4:
+        raise ValueError("expected query [B,H,D], key_cache [NB,Hk,D/x,bs,x], value_cache [NB,Hk,D,bs]")
+    a = DecodeArgs()
+    a.num_seqs, a.num_heads, a.head_size = query.shape
+    a.num_kv_heads = key_cache.shape[1]
+    a.block_size = key_cache.shape[3]
+    a.x = key_cache.shape[4]
+    a.num_blocks = key_cache.shape[0]
+    if kv_indptr is None:
+        if block_tables.dim() != 2:
+            raise ValueError("block_tables must be 2-D [num_seqs, max_blocks_per_seq]")
+        a.max_blocks_per_seq = block_tables.shape[1] if max_blocks_per_seq is None else max_blocks_per_seq
+        a.bt_stride[0], a.bt_stride[1] = block_tables.stride()
+    else:
+        if block_tables.dim() != 1:
+            raise ValueError("with kv_indptr, block_tables is the flat page list (1-D)")
+        a.max_blocks_per_seq = 0 if max_blocks_per_seq is None else max_blocks_per_seq
+        a.bt_stride[0], a.bt_stride[1] = 0, block_tables.stride(0)
+    a.dtype = _DTYPE_CODE[query.dtype]
+    a.scale = float(scale)
+    a.query = _ptr(query)
+    for i, s in enumerate(query.stride()):
+        a.q_stride[i] = s
+    a.key_cache = _ptr(key_cache)
+    for i, s in enumerate(key_cache.stride()):
+        a.k_stride[i] = s
+    a.value_cache = _ptr(value_cache)
+    for i, s in enumerate(value_cache.stride()):
+        a.v_stride[i] = s
+    a.block_tables = _ptr(block_tables)
+    a.kv_indptr = _ptr(kv_indptr)
+    a.seq_lens = _ptr(seq_lens)
+    a.err_flag = _ptr(err_flag)
+    return a
+
+
+def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                           value_cache: torch.Tensor, block_tables: torch.Tensor,
+                           seq_lens: torch.Tensor, scale: float, *,
+                           kv_indptr: Optional[torch.Tensor] = None,
+                           err_flag: Optional[torch.Tensor] = None,
+                           max_blocks_per_seq: Optional[int] = None, stream=None) -> None:
+    """Single-pass decode into ``out [num_seqs, num_heads, head_size]`` (query's dtype)."""
+    _cuda(out, "out")
+    if out.dtype != query.dtype or tuple(out.shape) != tuple(query.shape):
+        raise ValueError("out must match query's shape and dtype")
+    a = _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
+                     err_flag, max_blocks_per_seq)
+    os_ = _I64x3(*out.stride())
+    _check(lib().paged_attention_decode(_ptr(out), os_, ctypes.byref(a), _stream(stream)),
+           "paged_attention_decode")
+
+
+def paged_attention_v2_partition(tmp_out: torch.Tensor, exp_sums: torch.Tensor,
+                                 max_logits: torch.Tensor, query: torch.Tensor,
+                                 key_cache: torch.Tensor, value_cache: torch.Tensor,
+                                 block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                                 *, partition_size: int = 512,
+                                 num_kv_splits: Optional[torch.Tensor] = None,
+                                 kv_indptr: Optional[torch.Tensor] = None,
+                                 err_flag: Optional[torch.Tensor] = None,
+                                 max_blocks_per_seq: Optional[int] = None, stream=None) -> None:
+    """Split-KV partition pass; ``tmp_out [B,H,maxP,D]``, ``exp_sums``/``max_logits [B,H,maxP]`` fp32."""
+    for t, n in ((tmp_out, "tmp_out"), (exp_sums, "exp_sums"), (max_logits, "max_logits"),
+                 (num_kv_splits, "num_kv_splits")):
+        _cuda(t, n)
+    for t in (tmp_out, exp_sums, max_logits):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("tmp_out, exp_sums and max_logits must be contiguous float32")
+    B, H, maxP, D = tmp_out.shape
+    if (B, H, D) != tuple(query.shape) or tuple(exp_sums.shape) != (B, H, maxP) or \
+            tuple(max_logits.shape) != (B, H, maxP):
+        raise ValueError("scratch shapes do not match the query")
+    if num_kv_splits is not None and num_kv_splits.dtype != torch.int32:
+        raise ValueError("num_kv_splits must be int32")
+    a = _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
+                     err_flag, max_blocks_per_seq)
+    _check(lib().paged_attention_v2_partition(_ptr(tmp_out), _ptr(exp_sums), _ptr(max_logits),
+                                              maxP, int(partition_size), _ptr(num_kv_splits),
+                                              ctypes.byref(a), _stream(stream)),
+           "paged_attention_v2_partition")
+
+
+def paged_attention_v2_reduce(out: torch.Tensor, tmp_out: torch.Tensor, exp_sums: torch.Tensor,
+                              max_logits: torch.Tensor, seq_lens: torch.Tensor, *,
+                              partition_size: int = 512,
+                              num_kv_splits: Optional[torch.Tensor] = None, block_size: int = 16,
+                              err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Log-sum-exp combination of the partitions into ``out [B, H, D]``."""
+    for t, n in ((out, "out"), (tmp_out, "tmp_out"), (exp_sums, "exp_sums"),
+                 (max_logits, "max_logits"), (seq_lens, "seq_lens"),
+                 (num_kv_splits, "num_kv_splits"), (err_flag, "err_flag")):
+        _cuda(t, n)
+    if out.dtype not in _DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {out.dtype}")
+    for t in (tmp_out, exp_sums, max_logits):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("tmp_out, exp_sums and max_logits must be contiguous float32")
+    B, H, maxP, D = tmp_out.shape
+    if tuple(out.shape) != (B, H, D):
+        raise ValueError("out must be [num_seqs, num_heads, head_size]")
+    os_ = _I64x3(*out.stride())
+    _check(lib().paged_attention_v2_reduce(_ptr(out), os_, _ptr(tmp_out), _ptr(exp_sums),
+                                           _ptr(max_logits), _ptr(seq_lens), _ptr(num_kv_splits),
+                                           B, H, D, int(block_size), maxP, int(partition_size),
+                                           _DTYPE_CODE[out.dtype], _ptr(err_flag),
+                                           _stream(stream)),
+           "paged_attention_v2_reduce")
+
+
+def copy_page_indices(page_indices: torch.Tensor, block_table: torch.Tensor,
+                      cu_num_blocks: torch.Tensor, *, err_flag: Optional[torch.Tensor] = None,
+                      stream=None) -> None:
+    """``page_indices[cu[i] + j] = block_table[i, j]`` for ``j < cu[i+1] - cu[i]`` (any strides)."""
+    for t, n in ((page_indices, "page_indices"), (block_table, "block_table"),
+                 (cu_num_blocks, "cu_num_blocks"), (err_flag, "err_flag")):
+        _cuda(t, n)
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    if block_table.dim() != 2 or cu_num_blocks.dim() != 1 or page_indices.dim() != 1:
+        raise ValueError("expected block_table [R, C], cu_num_blocks [R+1], page_indices [N]")
+    if not page_indices.is_contiguous() or not cu_num_blocks.is_contiguous():
+        raise ValueError("page_indices and cu_num_blocks must be contiguous")
+    R = cu_num_blocks.shape[0] - 1
+    if R > block_table.shape[0]:
+        raise ValueError("cu_num_blocks has more rows than block_table")
+    s0, s1 = block_table.stride()
+    _check(lib().copy_page_indices(_ptr(page_indices), page_indices.numel(), _ptr(block_table),
+                                   block_table.shape[1], s0, s1, _ptr(cu_num_blocks), R,
+                                   _ptr(err_flag), _stream(stream)),
+           "copy_page_indices")
+
+
+def compute_num_kv_splits(num_kv_splits: torch.Tensor, seq_lens: torch.Tensor, *, num_group: int,
+                          num_head: int, num_kv_head: int, max_kv_splits: int,
+                          device_core_count: int, stream=None) -> None:
+    """Per-sequence split count into ``num_kv_splits [num_seq * num_group]`` (int32)."""
+    for t, n in ((num_kv_splits, "num_kv_splits"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous int32")
+    n = seq_lens.numel()
+    if num_kv_splits.numel() < n * num_group:
+        raise ValueError("num_kv_splits is too small")
+    _check(lib().compute_num_kv_splits(_ptr(num_kv_splits), _ptr(seq_lens), n, int(num_group),
+                                       int(num_head), int(num_kv_head), int(max_kv_splits),
+                                       int(device_core_count), _stream(stream)),
+           "compute_num_kv_splits")

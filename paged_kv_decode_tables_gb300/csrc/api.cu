@@ -1,0 +1,277 @@
+// C ABI of the paged-KV decode library: argument checks on the host, instance
+// selection, launch on the caller's stream.  No allocation, no host sync.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/paged_kv.h"
+#include "attention_launch.cuh"
+#include "metadata.cuh"
+#include "reduce.cuh"
+
+namespace {
+
+using pkv::AttnParams;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_forced_warps{0};
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int v = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    v = 148;
+  g_sm_count[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+int elem_size(pkv_dtype_t t) {
+  switch (t) {
+    case PKV_F32: return 4;
+    case PKV_F16: return 2;
+    case PKV_BF16: return 2;
+    default: return 0;
+  }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_bytes16(int64_t stride, int elem) {
+  const int64_t b = stride * elem;
+  return (b % 16) == 0;
+}
+
+size_t smem_for(pkv_dtype_t t, int D, int BS, int W) {
+  switch (t) {
+    case PKV_F32: return pkv::smem_attention_f32(D, BS, W);
+    case PKV_F16: return pkv::smem_attention_f16(D, BS, W);
+    case PKV_BF16: return pkv::smem_attention_bf16(D, BS, W);
+    default: return 0;
+  }
+}
+
+// Checks shared by decode and the v2 partition pass.
+pkv_status_t check_decode_args(const pkv_decode_args_t *a) {
+  if (a == nullptr) return PKV_ERR_INVALID_ARG;
+  const int es = elem_size(a->dtype);
+  if (es == 0) return PKV_ERR_INVALID_ARG;
+  if (a->num_seqs < 0 || a->num_heads < 1 || a->num_kv_heads < 1) return PKV_ERR_INVALID_ARG;
+  if (a->num_heads % a->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (a->x * es != 16) return PKV_ERR_INVALID_ARG;
+  if (a->head_size < 1 || a->head_size % a->x != 0) return PKV_ERR_INVALID_ARG;
+  if (a->block_size < 1 || a->max_blocks_per_seq < 0 || a->num_blocks < 1)
+    return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(a->scale)) return PKV_ERR_INVALID_ARG;
+  if (a->num_seqs > 65535 || a->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (a->num_heads / a->num_kv_heads > pkv::kMaxGroup) return PKV_ERR_UNSUPPORTED;
+  if (smem_for(a->dtype, a->head_size, a->block_size, 1) == 0) return PKV_ERR_UNSUPPORTED;
+  if (a->num_seqs == 0) return PKV_OK;
+  if (!a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->seq_lens)
+    return PKV_ERR_INVALID_ARG;
+  // Each (block, kv_head) page must be one contiguous run.
+  const int64_t *ks = a->k_stride, *vs = a->v_stride;
+  if (ks[4] != 1 || ks[3] != a->x || ks[2] != int64_t(a->block_size) * a->x)
+    return PKV_ERR_UNSUPPORTED;
+  if (vs[3] != 1 || vs[2] != a->block_size) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(a->key_cache) || !aligned16(a->value_cache)) return PKV_ERR_INVALID_ARG;
+  if (!stride_bytes16(ks[0], es) || !stride_bytes16(ks[1], es) || !stride_bytes16(vs[0], es) ||
+      !stride_bytes16(vs[1], es))
+    return PKV_ERR_INVALID_ARG;
+  return PKV_OK;
+}
+
+AttnParams make_params(const pkv_decode_args_t *a) {
+  AttnParams p{};
+  p.q = a->query;
+  p.q_s0 = a->q_stride[0];
+  p.q_s1 = a->q_stride[1];
+  p.q_s2 = a->q_stride[2];
+  p.k = a->key_cache;
+  p.k_s0 = a->k_stride[0];
+  p.k_s1 = a->k_stride[1];
+  p.v = a->value_cache;
+  p.v_s0 = a->v_stride[0];
+  p.v_s1 = a->v_stride[1];
+  p.bt = a->block_tables;
+  p.bt_s0 = a->bt_stride[0];
+  p.bt_s1 = a->bt_stride[1];
+  p.indptr = a->kv_indptr;
+  p.seq_lens = a->seq_lens;
+  p.err = a->err_flag;
+  p.num_heads = a->num_heads;
+  p.num_kv_heads = a->num_kv_heads;
+  p.group = a->num_heads / a->num_kv_heads;
+  p.num_blocks = a->num_blocks;
+  p.max_blocks_per_seq = a->max_blocks_per_seq;
+  p.scale_log2 = a->scale * 1.44269504088896340736f;
+  return p;
+}
+
+// Warps per CTA: one warp per work unit when there are enough units to fill
+// every SM several times over, four (splitting the unit's chunks) otherwise.
+int pick_warps(const pkv_decode_args_t *a, int64_t units) {
+  const int forced = g_forced_warps.load(std::memory_order_relaxed);
+  if (forced == 1 || forced == 4) {
+    if (smem_for(a->dtype, a->head_size, a->block_size, forced) != 0) return forced;
+  }
+  const bool four_ok = smem_for(a->dtype, a->head_size, a->block_size, 4) != 0;
+  if (!four_ok) return 1;
+  return units >= int64_t(sm_count()) * 16 ? 1 : 4;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_version(void) { return "paged_kv 0.1.0 sm_103a"; }
+
+const char *pkv_status_string(pkv_status_t s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape, dtype or layout";
+    case PKV_ERR_CUDA: return "CUDA launch error";
+    default: return "unknown status";
+  }
+}
+
+size_t pkv_decode_args_size(void) { return sizeof(pkv_decode_args_t); }
+
+pkv_status_t pkv_set_attention_warps(int32_t warps) {
+  if (warps != 0 && warps != 1 && warps != 4) return PKV_ERR_INVALID_ARG;
+  g_forced_warps.store(warps, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
+                                    const pkv_decode_args_t *args, pkv_stream_t stream) {
+  pkv_status_t st = check_decode_args(args);
+  if (st != PKV_OK) return st;
+  if (!out || !out_stride) return PKV_ERR_INVALID_ARG;
+  if (args->num_seqs == 0) return PKV_OK;
+  AttnParams p = make_params(args);
+  p.mode = pkv::kModeV1;
+  p.out = out;
+  p.o_s0 = out_stride[0];
+  p.o_s1 = out_stride[1];
+  p.o_s2 = out_stride[2];
+  p.max_parts = 1;
+  dim3 grid(1, args->num_kv_heads, args->num_seqs);
+  const int w = pick_warps(args, int64_t(args->num_kv_heads) * args->num_seqs);
+  return pkv::launch_attention(args->dtype, p, args->head_size, args->block_size, w, grid,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float *max_logits,
+                                          int32_t max_num_partitions, int32_t partition_size,
+                                          const int32_t *num_kv_splits,
+                                          const pkv_decode_args_t *args, pkv_stream_t stream) {
+  pkv_status_t st = check_decode_args(args);
+  if (st != PKV_OK) return st;
+  if (!tmp_out || !exp_sums || !max_logits) return PKV_ERR_INVALID_ARG;
+  if (max_num_partitions < 1) return PKV_ERR_INVALID_ARG;
+  if (num_kv_splits == nullptr) {
+    if (partition_size < args->block_size || partition_size % args->block_size != 0)
+      return PKV_ERR_INVALID_ARG;
+    const int64_t need =
+        (int64_t(args->max_blocks_per_seq) * args->block_size + partition_size - 1) /
+        partition_size;
+    if (args->kv_indptr == nullptr && need > max_num_partitions) return PKV_ERR_INVALID_ARG;
+  }
+  if (args->num_seqs == 0) return PKV_OK;
+  AttnParams p = make_params(args);
+  p.mode = num_kv_splits ? pkv::kModeSplits : pkv::kModeFixed;
+  p.tmp = tmp_out;
+  p.es = exp_sums;
+  p.ml = max_logits;
+  p.max_parts = max_num_partitions;
+  p.partition_size = num_kv_splits ? 0 : partition_size;
+  p.splits = num_kv_splits;
+  dim3 grid(max_num_partitions, args->num_kv_heads, args->num_seqs);
+  const int64_t units = int64_t(max_num_partitions) * args->num_kv_heads * args->num_seqs;
+  const int w = pick_warps(args, units);
+  return pkv::launch_attention(args->dtype, p, args->head_size, args->block_size, w, grid,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status_t paged_attention_v2_reduce(void *out, const int64_t out_stride[3],
+                                       const float *tmp_out, const float *exp_sums,
+                                       const float *max_logits, const int32_t *seq_lens,
+                                       const int32_t *num_kv_splits, int32_t num_seqs,
+                                       int32_t num_heads, int32_t head_size, int32_t block_size,
+                                       int32_t max_num_partitions, int32_t partition_size,
+                                       pkv_dtype_t out_dtype, int32_t *err_flag,
+                                       pkv_stream_t stream) {
+  if (num_seqs < 0 || num_heads < 1 || elem_size(out_dtype) == 0) return PKV_ERR_INVALID_ARG;
+  if (head_size != 64 && head_size != 128 && head_size != 256) return PKV_ERR_UNSUPPORTED;
+  if (max_num_partitions < 1 || max_num_partitions > 4096) return PKV_ERR_INVALID_ARG;
+  if (num_kv_splits == nullptr ? partition_size < 1 : block_size < 1) return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !out_stride || !tmp_out || !exp_sums || !max_logits || !seq_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(tmp_out)) return PKV_ERR_INVALID_ARG;
+  pkv::ReduceParams p{};
+  p.out = out;
+  p.o_s0 = out_stride[0];
+  p.o_s1 = out_stride[1];
+  p.o_s2 = out_stride[2];
+  p.tmp = tmp_out;
+  p.es = exp_sums;
+  p.ml = max_logits;
+  p.seq_lens = seq_lens;
+  p.splits = num_kv_splits;
+  p.err = err_flag;
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.head_size = head_size;
+  p.block_size = block_size;
+  p.max_parts = max_num_partitions;
+  p.partition_size = partition_size;
+  return pkv::launch_reduce(p, out_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status_t copy_page_indices(int32_t *page_indices, int64_t page_indices_capacity,
+                               const int32_t *block_table, int32_t num_cols, int64_t bt_stride0,
+                               int64_t bt_stride1, const int32_t *cu_num_blocks, int32_t num_reqs,
+                               int32_t *err_flag, pkv_stream_t stream) {
+  if (num_reqs < 0 || num_cols < 0 || page_indices_capacity < 0) return PKV_ERR_INVALID_ARG;
+  if (num_reqs == 0) return PKV_OK;
+  if (!page_indices || !block_table || !cu_num_blocks) return PKV_ERR_INVALID_ARG;
+  return pkv::launch_copy_page_indices(page_indices, page_indices_capacity, block_table, num_cols,
+                                       bt_stride0, bt_stride1, cu_num_blocks, num_reqs, err_flag,
+                                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status_t compute_num_kv_splits(int32_t *num_kv_splits, const int32_t *seq_lens, int32_t num_seq,
+                                   int32_t num_group, int32_t num_head, int32_t num_kv_head,
+                                   int32_t max_kv_splits, int32_t device_core_count,
+                                   pkv_stream_t stream) {
+  if (!num_kv_splits || !seq_lens) return PKV_ERR_INVALID_ARG;
+  if (num_seq < 1 || num_group < 1 || num_head < 1 || num_kv_head < 1) return PKV_ERR_INVALID_ARG;
+  if (num_head < num_kv_head || max_kv_splits < 1 || device_core_count < 1)
+    return PKV_ERR_INVALID_ARG;
+  return pkv::launch_num_kv_splits(num_kv_splits, seq_lens, num_seq, num_group, num_head,
+                                   num_kv_head, max_kv_splits, device_core_count,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace pkv {
+
+pkv_status_t launch_attention(pkv_dtype_t dtype, const AttnParams &p, int head_size,
+                              int block_size, int warps, dim3 grid, cudaStream_t stream) {
+  switch (dtype) {
+    case PKV_F32: return launch_attention_f32(p, head_size, block_size, warps, grid, stream);
+    case PKV_F16: return launch_attention_f16(p, head_size, block_size, warps, grid, stream);
+    case PKV_BF16: return launch_attention_bf16(p, head_size, block_size, warps, grid, stream);
+    default: return PKV_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,558 @@
+// Paged decode attention kernel: single-pass (v1) and split-KV partition (v2).
+//
+// One CTA per (partition, kv_head, sequence).  The CTA serves every query
+// head of the kv head's GQA group at once, so each K/V byte crosses HBM once
+// (page "paged_attention_v2_triton.py": per instance, load Q, gather K/V of the
+// partition's tokens, QK^T, online softmax, weighted V; for GQA the group of
+// query heads shares the kv head).
+//
+// Data movement.  A (block, kv_head) page of either cache is one contiguous
+// run of head_size*block_size elements (4 KiB at bf16/128/16).  Each warp runs
+// its own multi-stage pipeline: its lane 0 issues cp.async.bulk copies of
+// whole K and V pages into the warp's shared-memory stages, tracked by one
+// mbarrier per stage, and the warp computes on stage i while stages i+1.. are
+// in flight.  Warp w of the CTA takes chunks w, w+WARPS, ... of the
+// partition's tokens (a chunk is 16 tokens or one page, whichever is larger).
+// Block ids are resolved once per 32 chunks: each lane loads the id of one
+// upcoming chunk from the block table and the issuing lane picks it up by
+// shuffle (the per-token global scratch of the Triton prototype on page
+// "Needs help on performance optimization" is not needed).  Whole pages are
+// copied, so no load carries a per-token mask; tokens past the end only get a
+// -inf logit.
+//
+// Arithmetic (fp16/bf16).  Scores are S^T = K Q^T on mma.sync m16n8k16: M =
+// 16 tokens (ldmatrix reads the x-packed key page directly, 16 B = 8 dims of
+// one token per row), N = 8 query heads of the group, K = head dims, fp32
+// accumulate.  The output is O^T = V^T P^T: M = 16 head dims (ldmatrix reads
+// the value page, whose rows are one dim's tokens), N = 8 heads, K = 16
+// tokens; the probabilities go in as a hi + lo pair of 16-bit values
+// (movmatrix turns the score accumulator layout into the B-operand layout),
+// which keeps their rounding error near fp32.  Softmax runs in the log2
+// domain with ex2; row maxima use warp shuffles.
+//
+// fp32 runs the same pipeline with a CUDA-core body (no fp32 tensor path).
+#pragma once
+
+#include <type_traits>
+
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+
+enum AttnMode : int { kModeV1 = 0, kModeFixed = 1, kModeSplits = 2 };
+
+struct AttnParams {
+  const void *q;
+  int64_t q_s0, q_s1, q_s2;
+  const void *k;
+  int64_t k_s0, k_s1;
+  const void *v;
+  int64_t v_s0, v_s1;
+  const int32_t *bt;
+  int64_t bt_s0, bt_s1;
+  const int32_t *indptr;
+  const int32_t *seq_lens;
+  int32_t *err;
+  int32_t num_heads, num_kv_heads, group, num_blocks, max_blocks_per_seq;
+  float scale_log2;  // scale * log2(e)
+  int32_t mode;
+  void *out;  // v1 output
+  int64_t o_s0, o_s1, o_s2;
+  float *tmp, *es, *ml;  // v2 outputs
+  int32_t max_parts, partition_size;
+  const int32_t *splits;
+};
+
+constexpr int kMaxGroup = 8;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+__host__ __device__ constexpr int clamp_int(int v, int lo, int hi) {
+  return v < lo ? lo : (v > hi ? hi : v);
+}
+
+template <typename T, int D, int BS, int WARPS>
+struct AttnCfg {
+  static constexpr int kElem = int(sizeof(T));
+  static constexpr int kX = 16 / kElem;
+  static constexpr int kChunk = BS >= 16 ? BS : 16;  // tokens per pipeline stage
+  static constexpr int kPagesPerChunk = kChunk / BS;
+  static constexpr int kMTiles = kChunk / 16;
+  static constexpr int kPageBytes = D * BS * kElem;    // one K (or V) page
+  static constexpr int kHalfStage = kChunk * D * kElem;  // K (or V) part of a stage
+  static constexpr int kStageBytes = 2 * kHalfStage;
+  static constexpr int kWarpBudget = 24 * 1024;
+  static constexpr int kStages = clamp_int(kWarpBudget / kStageBytes, 2, 8);
+  static constexpr int kWarpBytes = kStages * kStageBytes;
+  static constexpr int kEpiFloats = kMaxGroup * D + 2 * kMaxGroup;
+  static constexpr int kSmemBytes = WARPS * kWarpBytes + WARPS * kStages * 8;
+  static constexpr int kThreads = WARPS * 32;
+  static_assert(kEpiFloats * 4 <= kWarpBytes, "epilogue does not fit the warp's stages");
+  static_assert(D % 32 == 0 && BS % 8 == 0, "unsupported shape");
+  static_assert(kHalfStage % 16 == 0 && kPageBytes % 16 == 0, "bulk copies need 16 B");
+};
+
+template <typename T, int D, int BS, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+    paged_attention_kernel(const AttnParams p) {
+  using Cfg = AttnCfg<T, D, BS, WARPS>;
+  constexpr bool kMma = !std::is_same<T, float>::value;
+  constexpr int PPC = Cfg::kPagesPerChunk;
+  constexpr int CH = Cfg::kChunk;
+  constexpr int NST = Cfg::kStages;
+  constexpr unsigned FULL = 0xffffffffu;
+
+  const int part = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int seq = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = p.group;
+  const bool leader = threadIdx.x == 0;
+
+  // ---------------------------------------------------- work decomposition --
+  int L = p.seq_lens[seq];
+  int64_t row_base;
+  int64_t cap_pages;
+  if (p.indptr != nullptr) {
+    const int a = p.indptr[seq];
+    const int b = p.indptr[seq + 1];
+    row_base = a;
+    cap_pages = int64_t(b) - a;
+    if (a < 0 || cap_pages < 0) {
+      if (leader) flag_error(p.err, 8u);
+      row_base = 0;
+      cap_pages = 0;
+    }
+  } else {
+    row_base = int64_t(seq) * p.bt_s0;
+    cap_pages = p.max_blocks_per_seq;
+  }
+  if (L < 0 || int64_t(L) > cap_pages * BS) {
+    if (leader) flag_error(p.err, 2u);
+    L = L < 0 ? 0 : int(cap_pages * BS);
+  }
+
+  int64_t t0, t1;
+  if (p.mode == kModeV1) {
+    t0 = 0;
+    t1 = L;
+  } else if (p.mode == kModeFixed) {
+    if (int64_t(L) > int64_t(p.max_parts) * p.partition_size) {
+      if (leader) flag_error(p.err, 2u);
+      L = int(int64_t(p.max_parts) * p.partition_size);
+    }
+    t0 = int64_t(part) * p.partition_size;
+    t1 = min(t0 + p.partition_size, int64_t(L));
+  } else {
+    int n = p.splits[seq];
+    if (L > 0 && (n < 1 || n > p.max_parts)) {
+      if (leader) flag_error(p.err, 4u);
+      n = clamp_int(n, 1, p.max_parts);
+    }
+    int64_t c = BS;
+    if (L > 0 && n > 0) {
+      c = (int64_t(L) + n - 1) / n;
+      c = (c + BS - 1) / BS * BS;
+    }
+    t0 = int64_t(part) * c;
+    t1 = part < n ? min(t0 + c, int64_t(L)) : t0;
+  }
+
+  const int h0 = kvh * g;
+  if (t0 >= t1) {
+    if (p.mode == kModeV1) {
+      T *out = static_cast<T *>(p.out);
+      for (int i = threadIdx.x; i < g * D; i += blockDim.x) {
+        const int h = i / D, d = i % D;
+        out[int64_t(seq) * p.o_s0 + int64_t(h0 + h) * p.o_s1 + int64_t(d) * p.o_s2] =
+            from_f32<T>(0.f);
+      }
+    } else {
+      for (int h = threadIdx.x; h < g; h += blockDim.x) {
+        const int64_t idx = (int64_t(seq) * p.num_heads + h0 + h) * p.max_parts + part;
+        p.es[idx] = 0.f;
+        p.ml[idx] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- pipeline --
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t *wbase = smem + warp * Cfg::kWarpBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * Cfg::kWarpBytes) + warp * NST;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  const int ntok = int(t1 - t0);
+  const int nchunks = (ntok + CH - 1) / CH;
+  const int my_n = nchunks > warp ? (nchunks - warp + WARPS - 1) / WARPS : 0;
+  const int64_t page0 = t0 / BS;
+  const uint8_t *kbase =
+      static_cast<const uint8_t *>(p.k) + int64_t(kvh) * p.k_s1 * Cfg::kElem;
+  const uint8_t *vbase =
+      static_cast<const uint8_t *>(p.v) + int64_t(kvh) * p.v_s1 * Cfg::kElem;
+  const int64_t kblk = p.k_s0 * Cfg::kElem;
+  const int64_t vblk = p.v_s0 * Cfg::kElem;
+  const uint64_t policy = l2_policy_evict_first();
+
+  // Lane l holds the block ids of this warp's chunk (32*batch + l).
+  int ids_cur[PPC], ids_nxt[PPC];
+  auto load_ids = [&](int batch, int (&ids)[PPC]) {
+    const int i = batch * 32 + lane;
+    const int64_t c = warp + int64_t(WARPS) * i;
+#pragma unroll
+    for (int j = 0; j < PPC; ++j) {
+      int id = -1;
+      const int64_t lp = page0 + c * PPC + j;
+      if (i < my_n && lp * BS < t1) {
+        id = __ldg(p.bt + row_base + lp * p.bt_s1);
+        if (id < 0 || id >= p.num_blocks) {
+          flag_error(p.err, 1u);
+          id = 0;
+        }
+      }
+      ids[j] = id;
+    }
+  };
+  load_ids(0, ids_cur);
+  if (my_n > 32) load_ids(1, ids_nxt);
+  int batch_cur = 0;
+  int issued = 0;
+
+  auto issue_next = [&]() {
+    const int i = issued;
+    const int b = i >> 5;
+    if (b != batch_cur) {
+#pragma unroll
+      for (int j = 0; j < PPC; ++j) ids_cur[j] = ids_nxt[j];
+      batch_cur = b;
+      if (my_n > (b + 1) * 32) load_ids(b + 1, ids_nxt);
+    }
+    int id[PPC];
+#pragma unroll
+    for (int j = 0; j < PPC; ++j) id[j] = __shfl_sync(FULL, ids_cur[j], i & 31);
+    const int st = i % NST;
+    if (lane == 0) {
+      uint8_t *ks = wbase + st * Cfg::kStageBytes;
+      uint8_t *vs = ks + Cfg::kHalfStage;
+      uint32_t np = 0;
+#pragma unroll
+      for (int j = 0; j < PPC; ++j) np += id[j] >= 0 ? 1u : 0u;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bars[st], np * 2u * Cfg::kPageBytes);
+#pragma unroll
+      for (int j = 0; j < PPC; ++j) {
+        if (id[j] >= 0) {
+          bulk_copy_g2s(ks + j * Cfg::kPageBytes, kbase + int64_t(id[j]) * kblk, Cfg::kPageBytes,
+                        &bars[st], policy);
+          bulk_copy_g2s(vs + j * Cfg::kPageBytes, vbase + int64_t(id[j]) * vblk, Cfg::kPageBytes,
+                        &bars[st], policy);
+        }
+      }
+    }
+    ++issued;
+  };
+
+  const int prologue = my_n < NST ? my_n : NST;
+  for (int i = 0; i < prologue; ++i) issue_next();
+
+  // Per-warp softmax state and accumulators.
+  float *epi = reinterpret_cast<float *>(wbase);  // reused after the pipeline drains
+  bool ok = true;
+  int waited = 0;
+
+  if constexpr (kMma) {
+    constexpr int DT = D / 16;  // 16-dim tiles
+    // Q^T fragments (B operand): dims 16ks + 2(lane%4) (+1), (+8); head lane/4.
+    uint32_t qf[DT][2];
+    {
+      const int h = lane >> 2;
+      const uint16_t *qb = static_cast<const uint16_t *>(p.q) + int64_t(seq) * p.q_s0 +
+                           int64_t(h0 + h) * p.q_s1;
+#pragma unroll
+      for (int ks = 0; ks < DT; ++ks) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int d = 16 * ks + 2 * (lane & 3) + 8 * half;
+          uint32_t lo = 0, hi = 0;
+          if (h < g) {
+            lo = qb[int64_t(d) * p.q_s2];
+            hi = qb[int64_t(d + 1) * p.q_s2];
+          }
+          qf[ks][half] = lo | (hi << 16);
+        }
+      }
+    }
+    float acc[DT][4];
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+
+    const int jm = lane >> 3, rr = lane & 7;
+    for (int i = 0; i < my_n; ++i) {
+      const int st = i % NST;
+      const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u);
+      if (!__all_sync(FULL, got)) {
+        ok = false;
+        break;
+      }
+      waited = i + 1;
+      const int64_t c = warp + int64_t(WARPS) * i;
+      const int nv = int(min(int64_t(CH), t1 - (t0 + c * CH)));
+      uint8_t *ks = wbase + st * Cfg::kStageBytes;
+      uint8_t *vs = ks + Cfg::kHalfStage;
+      if (nv < CH) {
+        // Zero the value columns of tokens past the end: their probability
+        // is 0, but 0 * (stale or NaN) must not reach the accumulator.
+        T *vt = reinterpret_cast<T *>(vs);
+        const int ntail = CH - nv;
+        for (int e = lane; e < D * ntail; e += 32) {
+          const int d = e / ntail;
+          const int tau = nv + e % ntail;
+          vt[(tau / BS) * (D * BS) + d * BS + (tau % BS)] = from_f32<T>(0.f);
+        }
+        __syncwarp();
+      }
+      const uint32_t ks_a = smem_addr(ks);
+      const uint32_t vs_a = smem_addr(vs);
+
+      float x[Cfg::kMTiles][4];
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int tok = 16 * mt + rr + 8 * (jm & 1);
+        const uint32_t rowa =
+            ks_a + (tok / BS) * Cfg::kPageBytes + ((jm >> 1) * BS + (tok % BS)) * 16;
+#pragma unroll
+        for (int k2 = 0; k2 < DT; ++k2) {
+          uint32_t a[4];
+          ldsm_x4(rowa + k2 * (2 * BS * 16), a[0], a[1], a[2], a[3]);
+          if (k2 & 1)
+            Mma16816<T>::run(s1, a, qf[k2][0], qf[k2][1]);
+          else
+            Mma16816<T>::run(s0, a, qf[k2][0], qf[k2][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 16 * mt + (lane >> 2) + 8 * (e >> 1);
+          x[mt][e] = t < nv ? (s0[e] + s1[e]) * p.scale_log2 : -INFINITY;
+        }
+      }
+      float mloc[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        mloc[0] = fmaxf(mloc[0], fmaxf(x[mt][0], x[mt][2]));
+        mloc[1] = fmaxf(mloc[1], fmaxf(x[mt][1], x[mt][3]));
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mloc[0] = fmaxf(mloc[0], __shfl_xor_sync(FULL, mloc[0], o));
+        mloc[1] = fmaxf(mloc[1], __shfl_xor_sync(FULL, mloc[1], o));
+      }
+      float alpha[2], muse[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float mn = fmaxf(m_run[j], mloc[j]);
+        muse[j] = mn == -INFINITY ? 0.f : mn;
+        alpha[j] = ex2(m_run[j] - muse[j]);
+        m_run[j] = mn;
+      }
+      float pr[Cfg::kMTiles][4];
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[mt][e] = ex2(x[mt][e] - muse[e & 1]);
+      }
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        ls0 += pr[mt][0] + pr[mt][2];
+        ls1 += pr[mt][1] + pr[mt][3];
+      }
+      l_run[0] = l_run[0] * alpha[0] + ls0;
+      l_run[1] = l_run[1] * alpha[1] + ls1;
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) {
+        acc[dt][0] *= alpha[0];
+        acc[dt][1] *= alpha[1];
+        acc[dt][2] *= alpha[0];
+        acc[dt][3] *= alpha[1];
+      }
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        const uint32_t hi0 = pack2<T>(pr[mt][0], pr[mt][1]);
+        const uint32_t hi1 = pack2<T>(pr[mt][2], pr[mt][3]);
+        const float2 f0 = unpack2<T>(hi0), f1 = unpack2<T>(hi1);
+        const uint32_t lo0 = pack2<T>(pr[mt][0] - f0.x, pr[mt][1] - f0.y);
+        const uint32_t lo1 = pack2<T>(pr[mt][2] - f1.x, pr[mt][3] - f1.y);
+        const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
+        const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
+        const int tok0 = 16 * mt + 8 * (jm >> 1);
+        const uint32_t rowv = vs_a + (tok0 / BS) * Cfg::kPageBytes + (tok0 % BS) * 2 +
+                              (rr + 8 * (jm & 1)) * (BS * 2);
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          uint32_t a[4];
+          ldsm_x4(rowv + dt * (16 * BS * 2), a[0], a[1], a[2], a[3]);
+          Mma16816<T>::run(acc[dt], a, bh0, bh1);
+          Mma16816<T>::run(acc[dt], a, bl0, bl1);
+        }
+      }
+      __syncwarp();
+      if (issued < my_n) issue_next();
+    }
+
+    // Full per-head sums: lanes sharing lane%4 hold the same two heads.
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l_run[0] += __shfl_xor_sync(FULL, l_run[0], o);
+      l_run[1] += __shfl_xor_sync(FULL, l_run[1], o);
+    }
+    if (!ok) {
+      if (lane == 0) flag_error(p.err, 16u);
+      for (int i = waited; i < issued; ++i)
+        mbar_wait_bounded(&bars[i % NST], uint32_t(i / NST) & 1u, 100000000ull);
+      __syncwarp();
+    }
+    // Stage memory of this warp is free now: store O (as [head][dim]), m, l.
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = 16 * dt + (lane >> 2) + 8 * (e >> 1);
+        const int h = 2 * (lane & 3) + (e & 1);
+        epi[h * D + d] = acc[dt][e];
+      }
+    }
+    if (lane < 4) {
+      epi[kMaxGroup * D + 2 * lane] = m_run[0];
+      epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
+      epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
+      epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
+    }
+  } else {
+    // ------------------------------------------------ fp32 CUDA-core body --
+    constexpr int DL = D / 32;  // dims per lane: lane + 32*i
+    float qv[kMaxGroup][DL];
+    float acc[kMaxGroup][DL];
+    float m_run[kMaxGroup], l_run[kMaxGroup];
+    {
+      const float *qb = static_cast<const float *>(p.q) + int64_t(seq) * p.q_s0;
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+#pragma unroll
+        for (int i = 0; i < DL; ++i) {
+          qv[h][i] = h < g ? qb[int64_t(h0 + h) * p.q_s1 + int64_t(lane + 32 * i) * p.q_s2] : 0.f;
+          acc[h][i] = 0.f;
+        }
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.f;
+      }
+    }
+    for (int i = 0; i < my_n; ++i) {
+      const int st = i % NST;
+      const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u);
+      if (!__all_sync(FULL, got)) {
+        ok = false;
+        break;
+      }
+      waited = i + 1;
+      const int64_t c = warp + int64_t(WARPS) * i;
+      const int nv = int(min(int64_t(CH), t1 - (t0 + c * CH)));
+      const float *kf = reinterpret_cast<const float *>(wbase + st * Cfg::kStageBytes);
+      const float *vf = kf + CH * D;
+      for (int tau = 0; tau < nv; ++tau) {
+        const int pg = tau / BS, slot = tau % BS;
+        float kv[DL], vv[DL];
+#pragma unroll
+        for (int i2 = 0; i2 < DL; ++i2) {
+          const int d = lane + 32 * i2;
+          kv[i2] = kf[pg * (D * BS) + (d / 4) * (BS * 4) + slot * 4 + (d & 3)];
+          vv[i2] = vf[pg * (D * BS) + d * BS + slot];
+        }
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h) {
+          if (h < g) {
+            float part = 0.f;
+#pragma unroll
+            for (int i2 = 0; i2 < DL; ++i2) part = fmaf(qv[h][i2], kv[i2], part);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
+            const float xs = part * p.scale_log2;
+            const float mn = fmaxf(m_run[h], xs);
+            const float a = ex2(m_run[h] - mn);
+            const float pe = ex2(xs - mn);
+            l_run[h] = l_run[h] * a + pe;
+#pragma unroll
+            for (int i2 = 0; i2 < DL; ++i2) acc[h][i2] = fmaf(acc[h][i2], a, pe * vv[i2]);
+            m_run[h] = mn;
+          }
+        }
+      }
+      __syncwarp();
+      if (issued < my_n) issue_next();
+    }
+    if (!ok) {
+      if (lane == 0) flag_error(p.err, 16u);
+      for (int i = waited; i < issued; ++i)
+        mbar_wait_bounded(&bars[i % NST], uint32_t(i / NST) & 1u, 100000000ull);
+      __syncwarp();
+    }
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+#pragma unroll
+      for (int i = 0; i < DL; ++i) epi[h * D + lane + 32 * i] = acc[h][i];
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+        epi[kMaxGroup * D + h] = m_run[h];
+        epi[kMaxGroup * D + kMaxGroup + h] = l_run[h];
+      }
+    }
+  }
+
+  // ---------------------------------------------- combine warps, write out --
+  if constexpr (WARPS > 1) {
+    __syncthreads();
+  } else {
+    __syncwarp();
+  }
+  for (int idx = threadIdx.x; idx < g * D; idx += WARPS * 32) {
+    const int h = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float *ew = reinterpret_cast<const float *>(smem + w * Cfg::kWarpBytes);
+      M = fmaxf(M, ew[kMaxGroup * D + h]);
+    }
+    float Ls = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float *ew = reinterpret_cast<const float *>(smem + w * Cfg::kWarpBytes);
+      const float f = ex2(ew[kMaxGroup * D + h] - M);
+      Ls = fmaf(f, ew[kMaxGroup * D + kMaxGroup + h], Ls);
+      O = fmaf(f, ew[h * D + d], O);
+    }
+    const float r = __fdiv_rn(O, Ls);
+    if (p.mode == kModeV1) {
+      T *out = static_cast<T *>(p.out);
+      out[int64_t(seq) * p.o_s0 + int64_t(h0 + h) * p.o_s1 + int64_t(d) * p.o_s2] = from_f32<T>(r);
+    } else {
+      const int64_t row = (int64_t(seq) * p.num_heads + h0 + h) * p.max_parts + part;
+      p.tmp[row * D + d] = r;
+      if (d == 0) {
+        p.es[row] = Ls;
+        p.ml[row] = M * kLn2;
+      }
+    }
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,126 @@
+// Sync-free decode metadata kernels.
+//
+// copy_page_indices: vLLM PR 35765 ("AITER MLA backend: Avoid CPU sync in
+//   _build_decode"), _copy_page_indices_kernel with the review's stride_1
+//   change.  One CTA per request row; the row's columns are copied with a
+//   block-stride loop (coalesced stores, strided loads).
+// compute_num_kv_splits: sglang metadata.py, get_num_kv_splits_triton.  One
+//   CTA: block-wide max/min of the lengths, the split formula evaluated once,
+//   then every thread writes its sequences' counts.
+#include "metadata.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kCopyThreads = 128;
+constexpr int kSplitThreads = 1024;
+
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_page_indices_kernel(int32_t *__restrict__ out, int64_t capacity,
+                             const int32_t *__restrict__ bt, int32_t num_cols, int64_t s0,
+                             int64_t s1, const int32_t *__restrict__ cu, int32_t *err) {
+  const int i = blockIdx.x;
+  const int64_t start = cu[i];
+  int64_t n = int64_t(cu[i + 1]) - start;
+  if (start < 0 || n < 0 || n > num_cols) {
+    if (threadIdx.x == 0) flag_error(err, 8u);
+    if (start < 0) return;
+    n = n < 0 ? 0 : num_cols;
+  }
+  if (start + n > capacity) {
+    if (threadIdx.x == 0) flag_error(err, 8u);
+    n = capacity > start ? capacity - start : 0;
+  }
+  const int32_t *row = bt + int64_t(i) * s0;
+  int32_t *dst = out + start;
+  for (int64_t j = threadIdx.x; j < n; j += kCopyThreads) dst[j] = __ldg(row + j * s1);
+}
+
+__device__ __forceinline__ int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+__global__ void __launch_bounds__(kSplitThreads)
+    num_kv_splits_kernel(int32_t *__restrict__ out, const int32_t *__restrict__ seq_lens,
+                         int32_t num_seq, int32_t num_group, int32_t num_head,
+                         int32_t num_kv_head, int32_t max_kv_splits, int32_t core_count) {
+  __shared__ int red_max[kSplitThreads / 32], red_min[kSplitThreads / 32];
+  __shared__ int64_t chunk[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  int mx = 1, mn = 0x7fffffff;
+  for (int s = tid; s < num_seq; s += kSplitThreads) {
+    const int L = max(seq_lens[s], 1);
+    mx = max(mx, L);
+    mn = min(mn, L);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  }
+  if (lane == 0) {
+    red_max[warp] = mx;
+    red_min[warp] = mn;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kSplitThreads / 32; ++w) {
+      mx = max(mx, red_max[w]);
+      mn = min(mn, red_min[w]);
+    }
+    int64_t mx64 = mx, mn64 = mn;
+    if (mx64 * 8 < mn64 * 10) mn64 = mx64;
+    const int64_t s1 = min(cdiv64(mx64, mn64), int64_t(max_kv_splits));
+    const int64_t c1 = cdiv64(mx64, s1);
+    // The one float32 step: log2(max_len / 64) rounded to float32, times the
+    // core count in float32, truncated toward zero.
+    const float ext_len = __fdiv_rn(__int2float_rn(mx), 64.0f);
+    const float lg = __double2float_rn(log2(double(ext_len)));
+    const float prod = __fmul_rn(__int2float_rn(core_count), fmaxf(lg, 1.0f));
+    const int64_t ext = __float2int_rz(prod);
+    const int kv_group = num_head / num_kv_head;
+    int64_t token_grid;
+    if (kv_group == 1) {
+      token_grid = int64_t(num_seq) * num_group * num_head;
+    } else {
+      const int block_h = min(16, kv_group);
+      token_grid = int64_t(num_seq) * num_group * cdiv64(num_head, block_h);
+    }
+    const int64_t s2 = min(cdiv64(ext, token_grid), int64_t(max_kv_splits));
+    const int64_t c2 = cdiv64(mx64, s2);
+    chunk[0] = c1;
+    chunk[1] = c2;
+  }
+  __syncthreads();
+  const int64_t c1 = chunk[0], c2 = chunk[1];
+  for (int s = tid; s < num_seq; s += kSplitThreads) {
+    const int64_t L = max(seq_lens[s], 0);
+    const int v = int(max(cdiv64(L, c1), cdiv64(L, c2)));
+    for (int i = 0; i < num_group; ++i) out[int64_t(s) * num_group + i] = v;
+  }
+}
+
+}  // namespace
+
+pkv_status_t launch_copy_page_indices(int32_t *page_indices, int64_t capacity,
+                                      const int32_t *block_table, int32_t num_cols, int64_t s0,
+                                      int64_t s1, const int32_t *cu, int32_t num_reqs,
+                                      int32_t *err, cudaStream_t stream) {
+  if (num_reqs == 0) return PKV_OK;
+  copy_page_indices_kernel<<<num_reqs, kCopyThreads, 0, stream>>>(page_indices, capacity,
+                                                                 block_table, num_cols, s0, s1,
+                                                                 cu, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status_t launch_num_kv_splits(int32_t *out, const int32_t *seq_lens, int32_t num_seq,
+                                  int32_t num_group, int32_t num_head, int32_t num_kv_head,
+                                  int32_t max_kv_splits, int32_t core_count,
+                                  cudaStream_t stream) {
+  num_kv_splits_kernel<<<1, kSplitThreads, 0, stream>>>(out, seq_lens, num_seq, num_group,
+                                                        num_head, num_kv_head, max_kv_splits,
+                                                        core_count);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

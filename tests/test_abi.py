@@ -1,0 +1,165 @@
+"""The C-ABI library builds, loads and exports every symbol its header
+declares; host-side argument checks reject bad calls before any launch.
+No GPU is needed: every call here fails validation (or has nothing to do)
+before the library touches the CUDA runtime."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "paged_kv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_decode_tables_gb300 import _build
+    try:
+        _build.nvcc_path()
+    except RuntimeError:
+        pytest.skip("no CUDA toolkit")
+    _build.build()
+    import paged_kv_decode_tables_gb300 as pkv
+    return pkv.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+char\s*\*|pkv_status_t|size_t)\s*(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_five_operations():
+    names = declared_functions()
+    for n in ("paged_attention_decode", "paged_attention_v2_partition", "paged_attention_v2_reduce",
+              "copy_page_indices", "compute_num_kv_splits"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import paged_kv_decode_tables_gb300 as pkv
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", pkv.lib_path()], capture_output=True,
+                         text=True)
+    if out.returncode == 0:
+        exported = set(line.split()[-1] for line in out.stdout.splitlines() if line.strip())
+        for n in names:
+            assert n in exported, n
+
+
+def test_struct_layout_matches_binding(lib):
+    import paged_kv_decode_tables_gb300 as pkv
+    assert lib.pkv_decode_args_size() == ctypes.sizeof(pkv.DecodeArgs)
+    assert "sm_103a" in pkv.version()
+    assert lib.pkv_status_string(0) == b"ok"
+    assert lib.pkv_status_string(2).startswith(b"unsupported")
+
+
+def _args(**kw):
+    import paged_kv_decode_tables_gb300 as pkv
+    a = pkv.DecodeArgs()
+    a.num_seqs, a.num_heads, a.num_kv_heads, a.head_size = 2, 8, 2, 128
+    a.block_size, a.x, a.max_blocks_per_seq, a.num_blocks = 16, 8, 4, 32
+    a.dtype, a.scale = 2, 0.1
+    a.query = a.key_cache = a.value_cache = 0x1000
+    a.block_tables = a.seq_lens = 0x2000
+    a.k_stride[:] = [2 * 16 * 16 * 8, 16 * 16 * 8, 16 * 8, 8, 1]
+    a.v_stride[:] = [2 * 128 * 16, 128 * 16, 16, 1]
+    a.q_stride[:] = [8 * 128, 128, 1]
+    a.bt_stride[:] = [4, 1]
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _decode(lib, a, out=0x3000):
+    strides = (ctypes.c_int64 * 3)(8 * 128, 128, 1)
+    return lib.paged_attention_decode(out, strides, ctypes.byref(a) if a is not None else None, None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("num_heads", 7, 1),        # not a multiple of num_kv_heads
+    ("x", 4, 1),                # x * sizeof(bf16) != 16
+    ("head_size", 96, 2),       # not built
+    ("block_size", 24, 2),      # not built
+    ("num_kv_heads", 1, 1),     # 8 / 1 = group 8 is fine but head check below
+    ("query", None, 1),         # null pointer
+    ("seq_lens", None, 1),
+    ("num_blocks", 0, 1),
+    ("dtype", 7, 1),
+    ("scale", float("nan"), 1),
+])
+def test_decode_rejects_bad_arguments(lib, field, value, status):
+    if field == "num_kv_heads":
+        a = _args(num_heads=32, num_kv_heads=2)  # group 16 > 8: not built
+        assert _decode(lib, a) == 2
+        return
+    a = _args(**{field: value})
+    assert _decode(lib, a) == status
+
+
+def test_decode_rejects_noncontiguous_pages_and_misalignment(lib):
+    a = _args()
+    a.k_stride[3] = 16  # x-groups not packed
+    assert _decode(lib, a) == 2
+    a = _args()
+    a.v_stride[3] = 2
+    assert _decode(lib, a) == 2
+    a = _args(key_cache=0x1008)  # not 16-byte aligned
+    assert _decode(lib, a) == 1
+    a = _args()
+    a.k_stride[0] = a.k_stride[0] + 4  # 8-byte block stride
+    assert _decode(lib, a) == 1
+    assert _decode(lib, None) == 1
+    assert _decode(lib, _args(), out=0) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _decode(lib, _args(num_seqs=0)) == 0
+    assert lib.copy_page_indices(0, 0, 0, 0, 0, 0, 0, 0, None, None) == 0
+
+
+def test_partition_rejects_bad_partitioning(lib):
+    a = _args()
+    p = 0x4000
+    # partition size not a multiple of block_size
+    assert lib.paged_attention_v2_partition(p, p, p, 4, 24, None, ctypes.byref(a), None) == 1
+    # too few partitions for max_blocks_per_seq * block_size = 64 tokens at P = 16
+    assert lib.paged_attention_v2_partition(p, p, p, 3, 16, None, ctypes.byref(a), None) == 1
+    assert lib.paged_attention_v2_partition(0, p, p, 4, 16, None, ctypes.byref(a), None) == 1
+    assert lib.paged_attention_v2_partition(p, p, p, 0, 16, None, ctypes.byref(a), None) == 1
+
+
+def test_reduce_and_metadata_reject_bad_arguments(lib):
+    s = (ctypes.c_int64 * 3)(1, 1, 1)
+    p = 0x4000
+    assert lib.paged_attention_v2_reduce(p, s, p, p, p, p, None, 2, 8, 96, 16, 4, 512, 2, None,
+                                         None) == 2
+    assert lib.paged_attention_v2_reduce(p, s, p, p, p, p, None, 2, 8, 128, 16, 0, 512, 2, None,
+                                         None) == 1
+    assert lib.paged_attention_v2_reduce(p, s, p + 4, p, p, p, None, 2, 8, 128, 16, 4, 512, 2,
+                                         None, None) == 1
+    assert lib.compute_num_kv_splits(p, p, 0, 1, 32, 8, 16, 148, None) == 1
+    assert lib.compute_num_kv_splits(p, p, 4, 1, 4, 8, 16, 148, None) == 1
+    assert lib.compute_num_kv_splits(p, p, 4, 1, 32, 8, 0, 148, None) == 1
+    assert lib.compute_num_kv_splits(p, p, 4, 1, 32, 8, 16, 0, None) == 1
+    assert lib.copy_page_indices(0, 10, p, 4, 4, 1, p, 2, None, None) == 1
+    assert lib.pkv_set_attention_warps(3) == 1
+    assert lib.pkv_set_attention_warps(0) == 0
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+
+    import paged_kv_decode_tables_gb300 as pkv
+    q = torch.zeros(1, 1, 64)
+    with pytest.raises(ValueError):
+        pkv.paged_attention_decode(q, q, torch.zeros(1, 1, 16, 8, 4), torch.zeros(1, 1, 64, 8),
+                                   torch.zeros(1, 1, dtype=torch.int32),
+                                   torch.zeros(1, dtype=torch.int32), 0.1)

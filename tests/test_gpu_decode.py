@@ -1,0 +1,288 @@
+"""GPU parity of the attention kernels against the float64 oracle, through
+the C ABI, on small batches that span several pipeline chunks and partitions
+and end in ragged tails; plus the edge cases of the method."""
+import math
+
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_tables_gb300 as pkv
+import workloads
+from gpu_support import (assert_attention_close, assert_partials_close, on_device, run_v1,
+                         run_v2)
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_kv_decode_tables_gb300 import _build
+    _build.build()
+    yield
+    pkv.set_attention_warps(0)
+
+
+def _inputs(dtype, D, bs, H, Hk, lens, seed=0, **kw):
+    return workloads.make_inputs(num_heads=H, num_kv_heads=Hk, head_size=D, block_size=bs,
+                                 dtype=dtype, seq_lens=lens, seed=seed, **kw)
+
+
+def _oracle_v1(inp, **kw):
+    return oracle.decode_v1(inp["query"], inp["key_cache"], inp["value_cache"],
+                            inp["block_tables"], inp["seq_lens_list"], inp["scale"], **kw)
+
+
+# ------------------------------------------------------- worked example ---
+
+def test_worked_example_fp32_single_pass():
+    inp = workloads.make_workload("tiny_mha_fp32")
+    g = on_device(inp)
+    out = run_v1(g)
+    err = assert_attention_close(out, _oracle_v1(inp), torch.float32, "tiny fp32")
+    assert err <= 1e-5
+
+
+# ------------------------------------------------------- v1 parity grid ---
+
+V1_CASES = [
+    # dtype, D, bs, H, Hk
+    ("bf16", 128, 16, 32, 8),
+    ("bf16", 128, 16, 8, 1),
+    ("bf16", 128, 16, 8, 8),
+    ("bf16", 128, 8, 16, 4),
+    ("bf16", 128, 32, 16, 2),
+    ("bf16", 64, 16, 12, 4),
+    ("bf16", 256, 16, 8, 2),
+    ("f16", 128, 16, 32, 32),
+    ("f16", 128, 8, 8, 4),
+    ("f16", 64, 32, 6, 3),
+    ("f16", 256, 8, 4, 1),
+    ("f32", 64, 8, 4, 4),
+    ("f32", 128, 16, 8, 1),
+    ("f32", 64, 32, 6, 2),
+    ("f32", 128, 8, 16, 8),
+]
+
+
+@pytest.mark.parametrize("warps", [1, 4])
+@pytest.mark.parametrize("dtype,D,bs,H,Hk", V1_CASES)
+def test_single_pass_parity(dtype, D, bs, H, Hk, warps):
+    lens = [1, bs - 1, 16 * 5 + 3, 333, bs * 7, 1000]
+    inp = _inputs(dtype, D, bs, H, Hk, lens, seed=D + bs + H)
+    g = on_device(inp)
+    pkv.set_attention_warps(warps)
+    try:
+        out = run_v1(g)
+    finally:
+        pkv.set_attention_warps(0)
+    assert_attention_close(out, _oracle_v1(inp), DT[dtype], f"v1 {dtype} D{D} bs{bs} {H}/{Hk}")
+
+
+def test_single_pass_peaky_keys_bf16():
+    """1% of keys scaled x8: near one-hot softmax rows, outputs of order 1-3."""
+    inp = _inputs("bf16", 128, 16, 64, 8, [4000, 1500, 777], seed=5, peaky_fraction=0.01)
+    g = on_device(inp)
+    assert_attention_close(run_v1(g), _oracle_v1(inp), torch.bfloat16, "peaky v1")
+
+
+# ------------------------------------------------------------ split-KV ---
+
+@pytest.mark.parametrize("dtype,D,bs,H,Hk", [("bf16", 128, 16, 64, 8), ("f16", 128, 16, 8, 8),
+                                             ("bf16", 64, 8, 8, 2), ("f32", 128, 16, 8, 2),
+                                             ("bf16", 256, 32, 4, 1)])
+@pytest.mark.parametrize("P", [32, 64, 512])
+def test_v2_fixed_partitions_parity(dtype, D, bs, H, Hk, P):
+    if P % bs:
+        pytest.skip("partition size must be a multiple of block_size")
+    lens = [1, P - 1, P, P + 1, 3 * P + 17, 1100]
+    inp = _inputs(dtype, D, bs, H, Hk, lens, seed=P + D, peaky_fraction=0.01)
+    g = on_device(inp)
+    maxP = -(-inp["max_blocks_per_seq"] * bs // P)
+    tmp, es, ml, out = run_v2(g, maxP, partition_size=P)
+    rtmp, res, rml = oracle.v2_partition(inp["query"], inp["key_cache"], inp["value_cache"],
+                                         inp["block_tables"], lens, inp["scale"], maxP,
+                                         partition_size=P)
+    assert_partials_close(tmp, es, ml, rtmp, res, rml, f"v2 partials {dtype} P{P}")
+    assert_attention_close(out, _oracle_v1(inp), DT[dtype], f"v2 {dtype} P{P}")
+
+
+def test_v2_matches_single_pass_on_gpu():
+    inp = _inputs("bf16", 128, 16, 32, 8, [2000, 513, 1], seed=9)
+    g = on_device(inp)
+    ref = _oracle_v1(inp)
+    assert_attention_close(run_v1(g), ref, torch.bfloat16, "v1")
+    for P in (16, 128, 512, 2048):
+        maxP = -(-inp["max_blocks_per_seq"] * 16 // P)
+        _, _, _, v2 = run_v2(g, maxP, partition_size=P)
+        assert_attention_close(v2, ref, torch.bfloat16, f"v2 P{P}")
+
+
+def test_v2_with_split_counts_parity():
+    lens = [5, 2047, 2048, 2049, 9000, 130, 64]
+    inp = _inputs("bf16", 128, 16, 32, 8, lens, seed=11)
+    g = on_device(inp)
+    splits = torch.empty(len(lens), dtype=torch.int32, device="cuda")
+    pkv.compute_num_kv_splits(splits, g["seq_lens"], num_group=1, num_head=32, num_kv_head=8,
+                              max_kv_splits=16, device_core_count=148)
+    want = oracle.num_kv_splits(lens, 1, 32, 8, 16, 148)
+    assert splits.cpu().tolist() == want
+    tmp, es, ml, out = run_v2(g, 16, splits=splits)
+    rtmp, res, rml = oracle.v2_partition(inp["query"], inp["key_cache"], inp["value_cache"],
+                                         inp["block_tables"], lens, inp["scale"], 16,
+                                         num_kv_splits=want)
+    assert_partials_close(tmp, es, ml, rtmp, res, rml, "split partials")
+    assert_attention_close(out, _oracle_v1(inp), torch.bfloat16, "split-KV")
+
+
+def test_reduce_alone_on_oracle_partials():
+    """The reduce kernel fed with the oracle's partials (rounded to fp32)."""
+    lens = [1, 700, 2500, 0]
+    inp = _inputs("bf16", 128, 16, 8, 2, lens, seed=12)
+    maxP = 6
+    rtmp, res, rml = oracle.v2_partition(inp["query"], inp["key_cache"], inp["value_cache"],
+                                         inp["block_tables"], lens, inp["scale"], maxP,
+                                         partition_size=512)
+    ref = oracle.v2_reduce(rtmp, res, rml, lens, 16, partition_size=512)
+    tmp = torch.nan_to_num(rtmp, nan=12345.0).float().cuda()
+    out = torch.empty(4, 8, 128, dtype=torch.bfloat16, device="cuda")
+    pkv.paged_attention_v2_reduce(out, tmp, res.float().cuda(), rml.float().cuda(),
+                                  torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                  partition_size=512)
+    assert_attention_close(out, ref, torch.bfloat16, "reduce")
+    assert bool((out[3].float() == 0).all())
+
+
+# ------------------------------------------------------------ invariants ---
+
+def test_flat_page_list_equals_block_table_bitwise():
+    lens = [100, 1, 555, 2048, 17]
+    inp = _inputs("bf16", 128, 16, 32, 8, lens, seed=13, bt_col_step=2)
+    g = on_device(inp)
+    nblk = [len(r) for r in inp["block_rows"]]
+    cu = torch.tensor([0] + torch.tensor(nblk).cumsum(0).tolist(), dtype=torch.int32,
+                      device="cuda")
+    flat = torch.empty(int(cu[-1]), dtype=torch.int32, device="cuda")
+    pkv.copy_page_indices(flat, g["block_tables"], cu)
+    a = run_v1(g)
+    b = run_v1(g, block_tables=flat, kv_indptr=cu)
+    assert torch.equal(a, b)
+    _, _, _, c = run_v2(g, 8, partition_size=512)
+    _, _, _, d = run_v2(g, 8, partition_size=512, block_tables=flat, kv_indptr=cu)
+    assert torch.equal(c, d)
+
+
+def test_block_relabelling_is_bitwise_invariant():
+    lens = [1234, 77, 512]
+    inp = _inputs("bf16", 128, 16, 16, 4, lens, seed=14)
+    g = on_device(inp)
+    base = run_v1(g)
+    NB = inp["num_blocks"]
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(3)).cuda()
+    kc = torch.empty_like(g["key_cache"])
+    vc = torch.empty_like(g["value_cache"])
+    kc[perm] = g["key_cache"]
+    vc[perm] = g["value_cache"]
+    bt = g["block_tables"].clone()
+    m = bt >= 0
+    bt[m] = perm[bt[m].long()].to(torch.int32)
+    g2 = dict(g, key_cache=kc, value_cache=vc, block_tables=bt)
+    assert torch.equal(base, run_v1(g2))
+
+
+def test_gqa_heads_with_equal_queries_agree():
+    inp = _inputs("bf16", 128, 16, 32, 4, [900, 33], seed=15)
+    q = inp["query"].view(2, 4, 8, 128)
+    q.copy_(q[:, :, :1, :].clone().expand_as(q))  # every head of a group: the group's first query
+    g = on_device(inp)
+    out = run_v1(g).view(2, 4, 8, 128)
+    assert torch.equal(out, out[:, :, :1, :].expand_as(out))
+
+
+def test_unused_cache_slots_never_reach_the_output():
+    """NaN in every slot no sequence owns, including the tails of last pages."""
+    lens = [3, 17, 250, 1025]
+    inp = _inputs("bf16", 128, 16, 16, 4, lens, seed=16, unused_slot_fill=float("nan"))
+    g = on_device(inp)
+    ref = _oracle_v1(inp)
+    for warps in (1, 4):
+        pkv.set_attention_warps(warps)
+        try:
+            assert_attention_close(run_v1(g), ref, torch.bfloat16, f"NaN slots w{warps}")
+            _, _, _, out = run_v2(g, 8, partition_size=128)
+            assert_attention_close(out, ref, torch.bfloat16, f"NaN slots v2 w{warps}")
+        finally:
+            pkv.set_attention_warps(0)
+    inp32 = _inputs("f32", 64, 8, 4, 2, lens, seed=17, unused_slot_fill=float("nan"))
+    assert_attention_close(run_v1(on_device(inp32)), _oracle_v1(inp32), torch.float32, "NaN f32")
+
+
+def test_zero_length_sequences():
+    lens = [0, 5, 0, 300]
+    inp = _inputs("bf16", 128, 16, 8, 2, lens, seed=18)
+    g = on_device(inp)
+    out = run_v1(g)
+    assert bool((out[0] == 0).all()) and bool((out[2] == 0).all())
+    _, es, ml, out2 = run_v2(g, 4, partition_size=128)
+    assert bool((out2[0] == 0).all()) and bool((es[0] == 0).all())
+    assert bool((ml[0] == -math.inf).all())
+    ref = _oracle_v1(inp)
+    assert_attention_close(out, ref, torch.bfloat16, "zero-len v1")
+    assert_attention_close(out2, ref, torch.bfloat16, "zero-len v2")
+
+
+def test_single_token_returns_value_row():
+    inp = _inputs("bf16", 128, 16, 8, 8, [1, 1], seed=19)
+    g = on_device(inp)
+    out = run_v1(g)
+    for s in range(2):
+        blk = inp["block_rows"][s][0]
+        v0 = inp["value_cache"][blk, :, :, 0]  # [Hk, D]
+        assert torch.equal(out[s].cpu(), v0)
+
+
+def test_non_default_stream_and_strided_query():
+    inp = _inputs("f16", 128, 16, 16, 4, [600, 31], seed=20)
+    g = on_device(inp)
+    wide = torch.zeros(2, 16, 256, dtype=torch.float16, device="cuda")
+    wide[:, :, :128] = g["query"]
+    g["query"] = wide[:, :, :128]
+    out_wide = torch.zeros(2, 16, 256, dtype=torch.float16, device="cuda")
+    out = out_wide[:, :, 64:192]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pkv.paged_attention_decode(out, g["query"], g["key_cache"], g["value_cache"],
+                                   g["block_tables"], g["seq_lens"], g["scale"])
+    s.synchronize()
+    assert_attention_close(out, _oracle_v1(inp), torch.float16, "strided")
+    assert bool((out_wide[:, :, :64] == 0).all()) and bool((out_wide[:, :, 192:] == 0).all())
+
+
+# ------------------------------------------------------------ error flags ---
+
+def test_bad_device_data_sets_flags_without_faulting():
+    lens = [40, 300]
+    inp = _inputs("bf16", 128, 16, 8, 2, lens, seed=21)
+    g = on_device(inp)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bt = g["block_tables"].clone()
+    bt[1, 3] = inp["num_blocks"] + 100  # out-of-range block id
+    run_v1(g, err=err, block_tables=bt)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.PKV_ERRF_BLOCK_ID
+    err.zero_()
+    g2 = dict(g, seq_lens=torch.tensor([40, 10 ** 6], dtype=torch.int32, device="cuda"))
+    run_v1(g2, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.PKV_ERRF_SEQ_LEN
+    err.zero_()
+    splits = torch.tensor([0, 99], dtype=torch.int32, device="cuda")
+    run_v2(g, 4, splits=splits, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.PKV_ERRF_SPLITS
+    # the context is still usable
+    assert_attention_close(run_v1(g), _oracle_v1(inp), torch.bfloat16, "after errors")

@@ -1,0 +1,121 @@
+"""GPU metadata kernels, bit-exact against the oracle: the page-index copy
+(any strides, empty rows, untouched tail) and the split-count heuristic
+(hand-worked cases and an exhaustive sweep of the float32 step)."""
+import os
+
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_tables_gb300 as pkv
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_kv_decode_tables_gb300 import _build
+    _build.build()
+
+
+@pytest.mark.parametrize("col_step", [1, 2, 3])
+@pytest.mark.parametrize("R,W", [(1, 1), (7, 9), (64, 300), (512, 2048)])
+def test_copy_page_indices_bit_exact(R, W, col_step):
+    g = torch.Generator().manual_seed(R * 31 + W + col_step)
+    storage = torch.randint(-2 ** 31, 2 ** 31 - 1, (R, W * col_step), generator=g,
+                            dtype=torch.int64).to(torch.int32)
+    bt = storage[:, ::col_step]
+    n = torch.randint(0, W + 1, (R,), generator=g)
+    if R > 2:
+        n[1] = 0
+        n[-1] = W
+    cu = [0]
+    for v in n.tolist():
+        cu.append(cu[-1] + v)
+    cap = cu[-1] + 37
+    out = torch.full((cap,), -77, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.copy_page_indices(out, storage.cuda()[:, ::col_step],
+                          torch.tensor(cu, dtype=torch.int32, device="cuda"), err_flag=err)
+    want = oracle.copy_page_indices(bt, cu, cap, fill=-77)
+    assert out.cpu().tolist() == want
+    assert int(err.item()) == 0
+
+
+def test_copy_page_indices_flags_overlong_rows():
+    bt = torch.arange(12, dtype=torch.int32, device="cuda").view(3, 4)
+    cu = torch.tensor([0, 2, 9, 10], dtype=torch.int32, device="cuda")  # row 1 asks for 7 > 4
+    out = torch.full((10,), -1, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.copy_page_indices(out, bt, cu, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.PKV_ERRF_INDPTR
+    assert out[:6].cpu().tolist() == [0, 1, 4, 5, 6, 7]
+
+
+def _split_cases():
+    cases = []
+    for line in open(os.path.join(GOLDEN, "num_kv_splits_cases.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, lens, params, expected = [p.strip() for p in line.split("|")]
+        cases.append((name, [int(v) for v in lens.split()], [int(v) for v in params.split()],
+                      [int(v) for v in expected.split()]))
+    return cases
+
+
+def _gpu_splits(lens, ng, nh, nkv, mx, cores, lens_dev=None):
+    seq = torch.tensor(lens, dtype=torch.int32, device="cuda") if lens_dev is None else lens_dev
+    out = torch.full((len(lens) * ng,), -1, dtype=torch.int32, device="cuda")
+    pkv.compute_num_kv_splits(out, seq, num_group=ng, num_head=nh, num_kv_head=nkv,
+                              max_kv_splits=mx, device_core_count=cores)
+    return out
+
+
+@pytest.mark.parametrize("case", _split_cases(), ids=lambda c: c[0])
+def test_num_kv_splits_hand_worked(case):
+    name, lens, (ng, nh, nkv, mx, cores), want = case
+    assert _gpu_splits(lens, ng, nh, nkv, mx, cores).cpu().tolist() == want
+
+
+def test_num_kv_splits_random_batches():
+    g = torch.Generator().manual_seed(1)
+    for trial in range(60):
+        B = int(torch.randint(1, 3000, (1,), generator=g))
+        hi = [64, 4096, 1 << 17][trial % 3]
+        lens = torch.randint(0, hi, (B,), generator=g).tolist()
+        nh, nkv = [(32, 8), (64, 8), (32, 32), (16, 1), (28, 4), (40, 40)][trial % 6]
+        mx = [1, 4, 16, 64][trial % 4]
+        ng = 1 + trial % 3
+        got = _gpu_splits(lens, ng, nh, nkv, mx, 148).cpu().tolist()
+        assert got == oracle.num_kv_splits(lens, ng, nh, nkv, mx, 148), trial
+
+
+def test_num_kv_splits_float32_step_exhaustive():
+    """Every max_seq_len in [1, 2^18]: the GPU's split count equals the
+    oracle's in two single-sequence batches whose head counts are chosen
+    (from the oracle's float32 intermediate e) so that any difference in that
+    intermediate changes the output: token_grid = e gives 1 split iff the
+    GPU's value is <= e, token_grid = e - 1 gives 2 iff it is >= e."""
+    N = 1 << 18
+    lens = torch.arange(1, N + 1, dtype=torch.int32, device="cuda")
+    lib = pkv.lib()
+    out = torch.full((2 * N,), -1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    base_l, base_o = lens.data_ptr(), out.data_ptr()
+    want = []
+    for i in range(N):
+        L = i + 1
+        e = oracle.ext_device_core_count(L, 148)
+        for j, tg in enumerate((e, max(e - 1, 1))):
+            st = lib.compute_num_kv_splits(base_o + 4 * (2 * i + j), base_l + 4 * i, 1, 1, tg, tg,
+                                           1 << 30, 148, stream)
+            assert st == 0
+            want.append(oracle.num_kv_splits([L], 1, tg, tg, 1 << 30, 148)[0])
+    got = out.cpu().tolist()
+    bad = [(k // 2 + 1, got[k], want[k]) for k in range(2 * N) if got[k] != want[k]]
+    assert not bad, bad[:10]
