@@ -144,7 +144,7 @@ class DecodeStep:
     """Device buffers of one workload and the launches of one step, issued
     straight through the C ABI with argument structs prepared once."""
 
-    def __init__(self, name: str, seed: int, device):
+    def __init__(self, name: str, seed: int, device, num_seqs=None):
         import ctypes
 
         import paged_kv_decode_tables_gb300 as pkv
@@ -152,7 +152,8 @@ class DecodeStep:
         self.pkv = pkv
         self.lib = pkv.lib()
         self.name = name
-        inp = workloads.make_workload(name, seed=seed, device=device)
+        over = {} if num_seqs is None else {"num_seqs": num_seqs}
+        inp = workloads.make_workload(name, seed=seed, device=device, **over)
         self.inp = inp
         spec = inp["spec"]
         self.spec = spec
@@ -432,7 +433,9 @@ def run_ours(args):
         _build.build()
     if dist is not None:
         dist.barrier()
-    step = DecodeStep(args.workload, seed=rank, device="cuda")
+    step = DecodeStep(args.workload, seed=rank, device="cuda", num_seqs=args.num_seqs)
+    if args.warps:
+        step.pkv.set_attention_warps(args.warps)
     spec = step.spec
     flush = step.kv_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda") if flush else None
@@ -576,6 +579,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="smaller batch of the same workload (profiling captures only)")
+    ap.add_argument("--warps", type=int, default=0, choices=[0, 1, 2, 4],
+                    help="force warps per attention CTA (0: library default)")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

@@ -122,7 +122,7 @@ size_t pkv_decode_args_size(void);
  * Tuning knob for paged_attention_decode / paged_attention_v2_partition: warps
  * per CTA, i.e. how many warps split one (sequence, kv head, partition) unit.
  * 0 (default) picks per call from the number of units and the SM count;
- * 1 or 4 forces that value where the instance exists.  Process-wide.
+ * 1, 2 or 4 forces that value where the instance exists.  Process-wide.
  * Returns PKV_ERR_INVALID_ARG for any other value.
  */
 pkv_status_t pkv_set_attention_warps(int32_t warps);
@@ -188,7 +188,7 @@ pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float
  *
  *   out: [num_seqs, num_heads, head_size] in out_dtype with strides out_stride.
  *   tmp_out / exp_sums / max_logits: as written by paged_attention_v2_partition.
- *   head_size in {64, 128, 256}; max_num_partitions <= 4096.
+ *   head_size in {64, 128, 256}.
  */
 pkv_status_t paged_attention_v2_reduce(void *out, const int64_t out_stride[3],
                                        const float *tmp_out, const float *exp_sums,

@@ -115,7 +115,7 @@ AttnParams make_params(const pkv_decode_args_t *a) {
 // every SM several times over, four (splitting the unit's chunks) otherwise.
 int pick_warps(const pkv_decode_args_t *a, int64_t units) {
   const int forced = g_forced_warps.load(std::memory_order_relaxed);
-  if (forced == 1 || forced == 4) {
+  if (forced == 1 || forced == 2 || forced == 4) {
     if (smem_for(a->dtype, a->head_size, a->block_size, forced) != 0) return forced;
   }
   const bool four_ok = smem_for(a->dtype, a->head_size, a->block_size, 4) != 0;
@@ -142,7 +142,7 @@ const char *pkv_status_string(pkv_status_t s) {
 size_t pkv_decode_args_size(void) { return sizeof(pkv_decode_args_t); }
 
 pkv_status_t pkv_set_attention_warps(int32_t warps) {
-  if (warps != 0 && warps != 1 && warps != 4) return PKV_ERR_INVALID_ARG;
+  if (warps != 0 && warps != 1 && warps != 2 && warps != 4) return PKV_ERR_INVALID_ARG;
   g_forced_warps.store(warps, std::memory_order_relaxed);
   return PKV_OK;
 }
@@ -208,7 +208,7 @@ pkv_status_t paged_attention_v2_reduce(void *out, const int64_t out_stride[3],
                                        pkv_stream_t stream) {
   if (num_seqs < 0 || num_heads < 1 || elem_size(out_dtype) == 0) return PKV_ERR_INVALID_ARG;
   if (head_size != 64 && head_size != 128 && head_size != 256) return PKV_ERR_UNSUPPORTED;
-  if (max_num_partitions < 1 || max_num_partitions > 4096) return PKV_ERR_INVALID_ARG;
+  if (max_num_partitions < 1) return PKV_ERR_INVALID_ARG;
   if (num_kv_splits == nullptr ? partition_size < 1 : block_size < 1) return PKV_ERR_INVALID_ARG;
   if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;

@@ -45,7 +45,7 @@ pkv_status_t launch_instance(const AttnParams &p, dim3 grid, cudaStream_t stream
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// Instances are built for WARPS in {1, 4}; a 4-warp instance only when its
+// Instances are built for WARPS in {1, 2, 4}; a 4-warp instance only when its
 // shared memory stays within the per-CTA limit.
 template <typename T, int D, int BS, int W>
 constexpr bool instance_fits() {
@@ -55,6 +55,9 @@ constexpr bool instance_fits() {
 template <typename T, int D, int BS>
 pkv_status_t launch_bs(const AttnParams &p, int warps, dim3 grid, cudaStream_t stream) {
   if (warps == 1) return launch_instance<T, D, BS, 1>(p, grid, stream);
+  if constexpr (instance_fits<T, D, BS, 2>()) {
+    if (warps == 2) return launch_instance<T, D, BS, 2>(p, grid, stream);
+  }
   if constexpr (instance_fits<T, D, BS, 4>()) {
     if (warps == 4) return launch_instance<T, D, BS, 4>(p, grid, stream);
   }
@@ -64,6 +67,9 @@ pkv_status_t launch_bs(const AttnParams &p, int warps, dim3 grid, cudaStream_t s
 template <typename T, int D, int BS>
 size_t smem_bs(int warps) {
   if (warps == 1) return AttnCfg<T, D, BS, 1>::kSmemBytes;
+  if constexpr (instance_fits<T, D, BS, 2>()) {
+    if (warps == 2) return AttnCfg<T, D, BS, 2>::kSmemBytes;
+  }
   if constexpr (instance_fits<T, D, BS, 4>()) {
     if (warps == 4) return AttnCfg<T, D, BS, 4>::kSmemBytes;
   }

@@ -2,61 +2,71 @@
 // _paged_attn_v2_reduce_kernel): global max of the partitions' max logits,
 // weights w_p = exp(m_p - M) * s_p, output = sum_p w_p tmp_p / sum_p w_p.
 //
-// One CTA per (query head, sequence); no host sync, no inter-CTA waiting.
-// Pass 1 finds M with warp shuffles; pass 2 stores the weights in shared
-// memory and sums them; pass 3 streams the fp32 partial outputs with float4
-// loads, the CTA's warps splitting the partitions, and combines the warps'
-// sums in shared memory.
+// One warp per (sequence, query head), eight per CTA; no host sync, no
+// shared memory and no inter-CTA waiting.  Lane l owns head dims
+// [l*D/32, (l+1)*D/32) of the output.  The warp takes the maximum with
+// shuffles, then walks the partitions 32 at a time: each lane computes one
+// partition's weight, the weights are broadcast by shuffle and every lane
+// accumulates its slice of the fp32 partial rows (one coalesced row read per
+// partition).
 #include "reduce.cuh"
 
 namespace pkv {
 
 namespace {
 
-constexpr int kReduceThreads = 256;
+constexpr int kReduceWarps = 8;
 constexpr float kLog2e = 1.44269504088896340736f;
+constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ float block_reduce_max(float v, float *red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = -INFINITY;
-  for (int w = 0; w < kReduceThreads / 32; ++w) r = fmaxf(r, red[w]);
-  return r;
-}
-
-__device__ __forceinline__ float block_reduce_sum(float v, float *red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = 0.f;
-  for (int w = 0; w < kReduceThreads / 32; ++w) r += red[w];
-  return r;
-}
+template <int V>
+struct Row;  // V consecutive floats of a partial row
+template <>
+struct Row<2> {
+  static __device__ __forceinline__ void load(const float *p, float (&v)[2]) {
+    const float2 t = __ldg(reinterpret_cast<const float2 *>(p));
+    v[0] = t.x;
+    v[1] = t.y;
+  }
+};
+template <>
+struct Row<4> {
+  static __device__ __forceinline__ void load(const float *p, float (&v)[4]) {
+    const float4 t = __ldg(reinterpret_cast<const float4 *>(p));
+    v[0] = t.x;
+    v[1] = t.y;
+    v[2] = t.z;
+    v[3] = t.w;
+  }
+};
+template <>
+struct Row<8> {
+  static __device__ __forceinline__ void load(const float *p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x;
+    v[1] = a.y;
+    v[2] = a.z;
+    v[3] = a.w;
+    v[4] = b.x;
+    v[5] = b.y;
+    v[6] = b.z;
+    v[7] = b.w;
+  }
+};
 
 template <typename TO, int D>
-__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceParams p) {
-  constexpr int D4 = D / 4;                     // float4 columns per row
-  constexpr int ROWS = kReduceThreads / D4;     // partitions read in parallel
-  static_assert(kReduceThreads % D4 == 0, "bad D");
-  extern __shared__ float sh[];
-  float *w = sh;                                // [max_parts]
-  float *red = sh + p.max_parts;                // [8]
-  float4 *part_acc = reinterpret_cast<float4 *>(sh + p.smem_head_floats);  // [ROWS][D4]
-
-  const int h = blockIdx.x;
-  const int s = blockIdx.y;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p) {
+  constexpr int V = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = int64_t(blockIdx.x) * kReduceWarps + (threadIdx.x >> 5);
+  if (unit >= int64_t(p.num_seqs) * p.num_heads) return;
+  const int s = int(unit / p.num_heads);
+  const int h = int(unit % p.num_heads);
 
   int L = p.seq_lens[s];
   if (L < 0) {
-    if (tid == 0) flag_error(p.err, 2u);
+    if (lane == 0) flag_error(p.err, 2u);
     L = 0;
   }
   int num_parts;
@@ -65,7 +75,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
   } else {
     int n = p.splits[s];
     if (L > 0 && (n < 1 || n > p.max_parts)) {
-      if (tid == 0) flag_error(p.err, 4u);
+      if (lane == 0) flag_error(p.err, 4u);
       n = n < 1 ? 1 : p.max_parts;
     }
     if (L > 0) {
@@ -77,74 +87,59 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
     }
   }
   if (num_parts > p.max_parts) {
-    if (tid == 0) flag_error(p.err, 2u);
+    if (lane == 0) flag_error(p.err, 2u);
     num_parts = p.max_parts;
   }
   TO *out = static_cast<TO *>(p.out) + int64_t(s) * p.o_s0 + int64_t(h) * p.o_s1;
   if (num_parts == 0) {
-    for (int d = tid; d < D; d += kReduceThreads) out[int64_t(d) * p.o_s2] = from_f32<TO>(0.f);
+#pragma unroll
+    for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(0.f);
     return;
   }
 
-  const int64_t row = (int64_t(s) * p.num_heads + h) * p.max_parts;
+  const int64_t row = unit * p.max_parts;  // == (s * num_heads + h) * max_parts
   const float *ml = p.ml + row;
   const float *es = p.es + row;
 
-  float m = -INFINITY;
-  for (int i = tid; i < num_parts; i += kReduceThreads) m = fmaxf(m, ml[i]);
-  const float M = block_reduce_max(m, red);
+  float M = -INFINITY;
+  for (int i = lane; i < num_parts; i += 32) M = fmaxf(M, __ldg(ml + i));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
 
-  float sum = 0.f;
-  for (int i = tid; i < num_parts; i += kReduceThreads) {
-    const float wi = ex2((ml[i] - M) * kLog2e) * es[i];
-    w[i] = wi;
-    sum += wi;
-  }
-  const float S = block_reduce_sum(sum, red);  // also orders the w[] stores
-  const float inv = __fdiv_rn(1.f, S);
-
-  const int r = tid / D4, c4 = tid % D4;
-  const float4 *tmp = reinterpret_cast<const float4 *>(p.tmp + row * D);
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = r; i < num_parts; i += ROWS) {
-    const float4 t = __ldg(tmp + int64_t(i) * D4 + c4);
-    const float wi = w[i];
-    a.x = fmaf(wi, t.x, a.x);
-    a.y = fmaf(wi, t.y, a.y);
-    a.z = fmaf(wi, t.z, a.z);
-    a.w = fmaf(wi, t.w, a.w);
-  }
-  part_acc[r * D4 + c4] = a;
-  __syncthreads();
-  if (r == 0) {
-    float4 t = part_acc[c4];
-    for (int rr = 1; rr < ROWS; ++rr) {
-      const float4 u = part_acc[rr * D4 + c4];
-      t.x += u.x;
-      t.y += u.y;
-      t.z += u.z;
-      t.w += u.w;
+  float S = 0.f;
+  float acc[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) acc[k] = 0.f;
+  const float *tmp = p.tmp + row * D + lane * V;
+  for (int c0 = 0; c0 < num_parts; c0 += 32) {
+    const int i = c0 + lane;
+    float w = 0.f;
+    if (i < num_parts) w = ex2((__ldg(ml + i) - M) * kLog2e) * __ldg(es + i);
+    S += w;
+    const int n = min(32, num_parts - c0);
+    const float *t = tmp + int64_t(c0) * D;
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(kFull, w, j);
+      float v[V];
+      Row<V>::load(t + int64_t(j) * D, v);
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] = fmaf(wj, v[k], acc[k]);
     }
-    const int d = 4 * c4;
-    out[int64_t(d + 0) * p.o_s2] = from_f32<TO>(t.x * inv);
-    out[int64_t(d + 1) * p.o_s2] = from_f32<TO>(t.y * inv);
-    out[int64_t(d + 2) * p.o_s2] = from_f32<TO>(t.z * inv);
-    out[int64_t(d + 3) * p.o_s2] = from_f32<TO>(t.w * inv);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+  const float inv = __fdiv_rn(1.f, S);
+#pragma unroll
+  for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(acc[k] * inv);
 }
 
 template <typename TO, int D>
 pkv_status_t launch_d(const ReduceParams &p, cudaStream_t stream) {
-  constexpr int D4 = D / 4;
-  constexpr int ROWS = kReduceThreads / D4;
-  // w[max_parts] + red[8], rounded to 16 B, then ROWS*D4 float4
-  size_t head = (size_t(p.max_parts) + 8) * sizeof(float);
-  head = (head + 15) / 16 * 16;
-  const size_t smem = head + size_t(ROWS) * D4 * sizeof(float4);
-  ReduceParams q = p;
-  q.smem_head_floats = int(head / sizeof(float));
-  dim3 grid(p.num_heads, p.num_seqs);
-  reduce_kernel<TO, D><<<grid, kReduceThreads, smem, stream>>>(q);
+  const int64_t units = int64_t(p.num_seqs) * p.num_heads;
+  const int64_t blocks = (units + kReduceWarps - 1) / kReduceWarps;
+  if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+  reduce_kernel<TO, D><<<unsigned(blocks), kReduceWarps * 32, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -16,7 +16,6 @@ struct ReduceParams {
   const int32_t *splits;  // may be null: fixed partition_size
   int32_t *err;
   int32_t num_seqs, num_heads, head_size, block_size, max_parts, partition_size;
-  int32_t smem_head_floats;  // set by the launcher
 };
 
 pkv_status_t launch_reduce(const ReduceParams &p, pkv_dtype_t out_dtype, cudaStream_t stream);

@@ -213,7 +213,8 @@ def test_unused_cache_slots_never_reach_the_output():
         pkv.set_attention_warps(warps)
         try:
             assert_attention_close(run_v1(g), ref, torch.bfloat16, f"NaN slots w{warps}")
-            _, _, _, out = run_v2(g, 8, partition_size=128)
+            maxP = -(-inp["max_blocks_per_seq"] * 16 // 128)
+            _, _, _, out = run_v2(g, maxP, partition_size=128)
             assert_attention_close(out, ref, torch.bfloat16, f"NaN slots v2 w{warps}")
         finally:
             pkv.set_attention_warps(0)
