@@ -22,7 +22,6 @@ CPU baseline: the float64 oracle timed on a bounded sample on the host cores.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import math
@@ -64,11 +63,12 @@ def load_peak():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the attention kernel's sources (the kernel the traffic figure describes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_tables_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in ("attention_kernel.cuh", "pkv_ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 

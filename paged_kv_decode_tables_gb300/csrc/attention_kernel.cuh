@@ -80,7 +80,7 @@ struct AttnCfg {
   static constexpr int kPageBytes = D * BS * kElem;    // one K (or V) page
   static constexpr int kHalfStage = kChunk * D * kElem;  // K (or V) part of a stage
   static constexpr int kStageBytes = 2 * kHalfStage;
-  static constexpr int kWarpBudget = 24 * 1024;
+  static constexpr int kWarpBudget = 16 * 1024;
   static constexpr int kStages = clamp_int(kWarpBudget / kStageBytes, 2, 8);
   static constexpr int kWarpBytes = kStages * kStageBytes;
   static constexpr int kEpiFloats = kMaxGroup * D + 2 * kMaxGroup;

@@ -2,13 +2,14 @@
 // _paged_attn_v2_reduce_kernel): global max of the partitions' max logits,
 // weights w_p = exp(m_p - M) * s_p, output = sum_p w_p tmp_p / sum_p w_p.
 //
-// One warp per (sequence, query head), eight per CTA; no host sync, no
-// shared memory and no inter-CTA waiting.  Lane l owns head dims
-// [l*D/32, (l+1)*D/32) of the output.  The warp takes the maximum with
-// shuffles, then walks the partitions 32 at a time: each lane computes one
-// partition's weight, the weights are broadcast by shuffle and every lane
-// accumulates its slice of the fp32 partial rows (one coalesced row read per
-// partition).
+// Lane l of a warp owns head dims [l*D/32, (l+1)*D/32) of the output.  The
+// maximum goes round by shuffles; partitions are then taken 32 at a time:
+// each lane computes one partition's weight, the weights are broadcast by
+// shuffle and every lane accumulates its slice of the fp32 partial rows (one
+// coalesced row read per partition).  Up to 32 partitions: one warp per
+// (sequence, head), eight per CTA, no shared memory.  More: one CTA per
+// (sequence, head) whose eight warps take the groups of 32 in turn and add up
+// in shared memory.  No host sync and no inter-CTA waiting either way.
 #include "reduce.cuh"
 
 namespace pkv {
@@ -55,18 +56,12 @@ struct Row<8> {
   }
 };
 
-template <typename TO, int D>
-__global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p) {
-  constexpr int V = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int64_t unit = int64_t(blockIdx.x) * kReduceWarps + (threadIdx.x >> 5);
-  if (unit >= int64_t(p.num_seqs) * p.num_heads) return;
-  const int s = int(unit / p.num_heads);
-  const int h = int(unit % p.num_heads);
-
+// Non-empty partitions of sequence s, computed exactly as the partition
+// pass splits it (fixed size, or roundup(cdiv(L, n), block_size) tokens).
+__device__ __forceinline__ int count_parts(const ReduceParams &p, int s, bool report) {
   int L = p.seq_lens[s];
   if (L < 0) {
-    if (lane == 0) flag_error(p.err, 2u);
+    if (report) flag_error(p.err, 2u);
     L = 0;
   }
   int num_parts;
@@ -75,7 +70,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
   } else {
     int n = p.splits[s];
     if (L > 0 && (n < 1 || n > p.max_parts)) {
-      if (lane == 0) flag_error(p.err, 4u);
+      if (report) flag_error(p.err, 4u);
       n = n < 1 ? 1 : p.max_parts;
     }
     if (L > 0) {
@@ -87,37 +82,29 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
     }
   }
   if (num_parts > p.max_parts) {
-    if (lane == 0) flag_error(p.err, 2u);
+    if (report) flag_error(p.err, 2u);
     num_parts = p.max_parts;
   }
-  TO *out = static_cast<TO *>(p.out) + int64_t(s) * p.o_s0 + int64_t(h) * p.o_s1;
-  if (num_parts == 0) {
-#pragma unroll
-    for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(0.f);
-    return;
-  }
+  return num_parts;
+}
 
-  const int64_t row = unit * p.max_parts;  // == (s * num_heads + h) * max_parts
-  const float *ml = p.ml + row;
-  const float *es = p.es + row;
-
-  float M = -INFINITY;
-  for (int i = lane; i < num_parts; i += 32) M = fmaxf(M, __ldg(ml + i));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-
-  float S = 0.f;
-  float acc[V];
-#pragma unroll
-  for (int k = 0; k < V; ++k) acc[k] = 0.f;
-  const float *tmp = p.tmp + row * D + lane * V;
-  for (int c0 = 0; c0 < num_parts; c0 += 32) {
+// Accumulate partitions [c_begin, c_end) in steps of 32 (c_stride apart):
+// each lane weighs one partition of the group, the weights go round by
+// shuffle, every lane adds its V dims of each partial row.
+template <int D>
+__device__ __forceinline__ void accumulate_parts(const float *ml, const float *es,
+                                                 const float *tmp_lane, int num_parts, float M,
+                                                 int c_begin, int c_step, float (&acc)[D / 32],
+                                                 float &S) {
+  constexpr int V = D / 32;
+  const int lane = threadIdx.x & 31;
+  for (int c0 = c_begin; c0 < num_parts; c0 += c_step) {
     const int i = c0 + lane;
     float w = 0.f;
     if (i < num_parts) w = ex2((__ldg(ml + i) - M) * kLog2e) * __ldg(es + i);
     S += w;
     const int n = min(32, num_parts - c0);
-    const float *t = tmp + int64_t(c0) * D;
+    const float *t = tmp_lane + int64_t(c0) * D;
 #pragma unroll 4
     for (int j = 0; j < n; ++j) {
       const float wj = __shfl_sync(kFull, w, j);
@@ -127,6 +114,45 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
       for (int k = 0; k < V; ++k) acc[k] = fmaf(wj, v[k], acc[k]);
     }
   }
+}
+
+// One warp per (sequence, head): for up to a few dozen partitions.
+template <typename TO, int D>
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p) {
+  constexpr int V = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = int64_t(blockIdx.x) * kReduceWarps + (threadIdx.x >> 5);
+  if (unit >= int64_t(p.num_seqs) * p.num_heads) return;
+  const int s = int(unit / p.num_heads);
+  const int h = int(unit % p.num_heads);
+  const int num_parts = count_parts(p, s, lane == 0);
+  TO *out = static_cast<TO *>(p.out) + int64_t(s) * p.o_s0 + int64_t(h) * p.o_s1;
+  const int64_t row = unit * p.max_parts;  // == (s * num_heads + h) * max_parts
+  const float *tmp = p.tmp + row * D + lane * V;
+  if (num_parts <= 1) {
+    // One partition is already normalised: the output is its row.
+    float v[V];
+    if (num_parts == 1) {
+      Row<V>::load(tmp, v);
+    } else {
+#pragma unroll
+      for (int k = 0; k < V; ++k) v[k] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(v[k]);
+    return;
+  }
+  const float *ml = p.ml + row;
+  const float *es = p.es + row;
+  float M = -INFINITY;
+  for (int i = lane; i < num_parts; i += 32) M = fmaxf(M, __ldg(ml + i));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  float S = 0.f;
+  float acc[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) acc[k] = 0.f;
+  accumulate_parts<D>(ml, es, tmp, num_parts, M, 0, 32, acc, S);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
   const float inv = __fdiv_rn(1.f, S);
@@ -134,12 +160,70 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
   for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(acc[k] * inv);
 }
 
+// One CTA per (sequence, head), the eight warps taking groups of 32
+// partitions in turn: for long sequences cut into many partitions.
+template <typename TO, int D>
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_wide_kernel(const ReduceParams p) {
+  constexpr int V = D / 32;
+  __shared__ float red[kReduceWarps];
+  __shared__ float part_S[kReduceWarps];
+  __shared__ __align__(16) float part_acc[kReduceWarps][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t unit = blockIdx.x;
+  const int s = int(unit / p.num_heads);
+  const int h = int(unit % p.num_heads);
+  const int num_parts = count_parts(p, s, threadIdx.x == 0);
+  TO *out = static_cast<TO *>(p.out) + int64_t(s) * p.o_s0 + int64_t(h) * p.o_s1;
+  if (num_parts == 0) {
+    for (int d = threadIdx.x; d < D; d += kReduceWarps * 32) out[int64_t(d) * p.o_s2] = from_f32<TO>(0.f);
+    return;
+  }
+  const int64_t row = unit * p.max_parts;
+  const float *ml = p.ml + row;
+  const float *es = p.es + row;
+  float M = -INFINITY;
+  for (int i = threadIdx.x; i < num_parts; i += kReduceWarps * 32) M = fmaxf(M, __ldg(ml + i));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kReduceWarps; ++w) M = fmaxf(M, red[w]);
+  float S = 0.f;
+  float acc[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) acc[k] = 0.f;
+  accumulate_parts<D>(ml, es, p.tmp + row * D + lane * V, num_parts, M, 32 * warp,
+                      32 * kReduceWarps, acc, S);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+#pragma unroll
+  for (int k = 0; k < V; ++k) part_acc[warp][lane * V + k] = acc[k];
+  if (lane == 0) part_S[warp] = S;
+  __syncthreads();
+  float St = 0.f;
+#pragma unroll
+  for (int w = 0; w < kReduceWarps; ++w) St += part_S[w];
+  const float inv = __fdiv_rn(1.f, St);
+  for (int d = threadIdx.x; d < D; d += kReduceWarps * 32) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kReduceWarps; ++w) t += part_acc[w][d];
+    out[int64_t(d) * p.o_s2] = from_f32<TO>(t * inv);
+  }
+}
+
 template <typename TO, int D>
 pkv_status_t launch_d(const ReduceParams &p, cudaStream_t stream) {
   const int64_t units = int64_t(p.num_seqs) * p.num_heads;
-  const int64_t blocks = (units + kReduceWarps - 1) / kReduceWarps;
-  if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
-  reduce_kernel<TO, D><<<unsigned(blocks), kReduceWarps * 32, 0, stream>>>(p);
+  if (p.max_parts > 32) {
+    if (units > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    reduce_wide_kernel<TO, D><<<unsigned(units), kReduceWarps * 32, 0, stream>>>(p);
+  } else {
+    const int64_t blocks = (units + kReduceWarps - 1) / kReduceWarps;
+    if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    reduce_kernel<TO, D><<<unsigned(blocks), kReduceWarps * 32, 0, stream>>>(p);
+  }
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
