@@ -52,6 +52,22 @@ def env_rank():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """Largest value of ``x`` over all ranks (rank timing: the slowest rank
+    defines the step); identity without a process group."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job throughput: every rank moves its own batch's bytes (weak
+    scaling) within the slowest rank's time."""
+    return world * bytes_per_rank / seconds / 1e9
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -478,10 +494,7 @@ def run_ours(args):
     clk = clocks.stop() if clocks else None
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
 
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
 
     # end to end through host buffers (per step: H2D of the inputs, the step,
     # D2H of the output, host waits for it)
@@ -495,10 +508,7 @@ def run_ours(args):
     for _ in range(Ke):
         step.e2e_step(hin, hout)
     e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dist, "cuda")
     h2d, d2h = step.e2e_bytes(hin, hout)
 
     if rank != 0:
@@ -507,7 +517,7 @@ def run_ours(args):
         return 0
 
     ms_step = elapsed_ms / K
-    value = world * step.kv_bytes / (ms_step * 1e-3) / 1e9
+    value = aggregate_gbs(step.kv_bytes, world, ms_step * 1e-3)
     attn_sorted = sorted(attn_ms)
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     peak, peak_kind = load_peak()
@@ -558,7 +568,7 @@ def run_ours(args):
                                   round(attn_sorted[(9 * len(attn_sorted)) // 10] * 1e3, 2)],
         },
         "step_share": {"attention_kernel": round(attn_avg_ms / ms_step, 4)},
-        "e2e": {"value": round(world * step.kv_bytes / (e2e_s / Ke) / 1e9, 2), "unit": UNIT,
+        "e2e": {"value": round(aggregate_gbs(step.kv_bytes, world, e2e_s / Ke), 2), "unit": UNIT,
                 "us_per_step": round(e2e_s / Ke * 1e6, 2), "steps": Ke,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "K/V cache resident on the device; per-step inputs from pinned host memory"},

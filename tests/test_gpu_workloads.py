@@ -1,0 +1,83 @@
+"""Full-size workloads in the launch configuration bench.py times.
+
+Metadata outputs are compared in full (bit-exact); attention outputs on
+sampled sequences (first, last, shortest, longest and a few seeded picks) that
+the oracle computes one by one, and on properties that hold everywhere:
+every output is finite and, being a convex combination of value rows, lies
+within the range of the cache's values.
+"""
+import pytest
+import torch
+
+import bench
+import oracle
+from gpu_support import assert_attention_close, assert_partials_close
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_kv_decode_tables_gb300 import _build
+    _build.build()
+
+
+def _samples(lens, extra=3, seed=0):
+    n = len(lens)
+    order = sorted(range(n), key=lambda i: lens[i])
+    picks = {0, n - 1, order[0], order[-1]}
+    g = torch.Generator().manual_seed(seed)
+    for i in torch.randperm(n, generator=g)[:extra].tolist():
+        picks.add(i)
+    return sorted(picks)
+
+
+def _run_step(name):
+    step = bench.DecodeStep(name, seed=0, device="cuda")
+    step.run()
+    torch.cuda.synchronize()
+    return step
+
+
+@pytest.mark.parametrize("name", ["mha_v1_fp16", "gqa_v1_bf16", "long_v2_bf16", "ragged_v2_bf16",
+                                  "tiny_mha_fp32"])
+def test_full_size_workload(name):
+    step = _run_step(name)
+    inp, spec = step.inp, step.spec
+    out = step.out
+    assert bool(torch.isfinite(out).all()), "non-finite output"
+    vmax = float(inp["value_cache"].float().abs().max())
+    assert float(out.float().abs().max()) <= vmax + 1e-3
+
+    splits = None
+    if spec.mode == "v2_splits":
+        bt = inp["block_tables"].cpu()
+        cu = inp["cu_num_blocks"].cpu().tolist()
+        want_pi = oracle.copy_page_indices(bt, cu, cu[-1])
+        assert step.page_indices.cpu().tolist() == want_pi
+        splits = oracle.num_kv_splits(step.lens, 1, spec.num_heads, spec.num_kv_heads,
+                                      spec.max_kv_splits, spec.device_core_count)
+        assert step.splits.cpu().tolist() == splits
+
+    seqs = _samples(step.lens)
+    q, kc, vc, bt, lens = bench.oracle_sample_inputs(inp, seqs)
+    ref = oracle.decode_v1(q, kc, vc, bt, lens, inp["scale"])
+    got = out[torch.tensor(seqs, device=out.device)]
+    assert_attention_close(got, ref, DT[spec.dtype], f"{name} sampled outputs")
+
+    if spec.mode != "v1":
+        sel = torch.tensor(seqs, device=out.device)
+        if spec.mode == "v2_fixed":
+            maxP = step.maxP
+            rtmp, res, rml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], maxP,
+                                                 partition_size=spec.partition_size)
+        else:
+            maxP = step.maxP
+            rtmp, res, rml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], maxP,
+                                                 num_kv_splits=[splits[s] for s in seqs])
+        assert_partials_close(step.tmp[sel], step.es[sel], step.ml[sel], rtmp, res, rml,
+                              f"{name} sampled partials")
