@@ -57,7 +57,8 @@ typedef enum {
   PKV_OK = 0,
   PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent strides */
   PKV_ERR_UNSUPPORTED = 2, /* valid but not built: head_size, block_size, group, layout */
-  PKV_ERR_CUDA = 3         /* the CUDA runtime refused the launch */
+  PKV_ERR_CUDA = 3,        /* the CUDA runtime refused the launch */
+  PKV_ERR_SCRATCH_TOO_SMALL = 4 /* request exceeds paged_attention_v2_noalloc's fixed scratch */
 } pkv_status_t;
 
 /* Bits OR-ed into *err_flag by kernels that meet bad device data. */
@@ -240,6 +241,42 @@ pkv_status_t compute_num_kv_splits(int32_t *num_kv_splits, const int32_t *seq_le
                                    int32_t num_group, int32_t num_head, int32_t num_kv_head,
                                    int32_t max_kv_splits, int32_t device_core_count,
                                    pkv_stream_t stream);
+
+/*
+ * Split-KV decode (partition pass + reduce) that allocates nothing.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot call cudaMalloc: an engine that reserves all device memory up
+ * front and allows no allocation while serving, a plugin inside a host
+ * application that owns the CUDA allocator, or a latency-critical path where
+ * cudaMalloc/cudaFree would add an implicit synchronisation.
+ *
+ * Same result as paged_attention_v2_partition followed by
+ * paged_attention_v2_reduce (same arguments, same kernels), but the
+ * per-partition scratch lives in a fixed array inside the library: 32 MiB
+ * (pkv_noalloc_scratch_bytes()) of device memory that every GPU loading the
+ * library holds until the process exits.  A call needs
+ *   num_seqs * num_heads * max_num_partitions * (head_size + 2) * 4 bytes
+ * (each of the three regions rounded up to 256 B) and returns
+ * PKV_ERR_SCRATCH_TOO_SMALL, enqueuing nothing, when that exceeds the array.
+ *
+ *   out: [num_seqs, num_heads, head_size] in args->dtype with strides out_stride.
+ *   max_num_partitions, partition_size, num_kv_splits, args: as for
+ *       paged_attention_v2_partition.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array and it
+ * keeps the last call's contents (every value a call reads is written by the
+ * same call first): calls that overlap on the GPU, on different streams,
+ * race on it.
+ */
+pkv_status_t paged_attention_v2_noalloc(void *out, const int64_t out_stride[3],
+                                        int32_t max_num_partitions, int32_t partition_size,
+                                        const int32_t *num_kv_splits,
+                                        const pkv_decode_args_t *args, pkv_stream_t stream);
+/* Size in bytes of paged_attention_v2_noalloc's fixed scratch array. */
+size_t pkv_noalloc_scratch_bytes(void);
 
 #ifdef __cplusplus
 } /* extern "C" */

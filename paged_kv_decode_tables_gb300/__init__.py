@@ -29,12 +29,15 @@ __all__ = [
     "paged_attention_v2_reduce",
     "copy_page_indices",
     "compute_num_kv_splits",
+    "paged_attention_v2_noalloc",
+    "noalloc_scratch_bytes",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(HERE, "libpaged_kv.so")
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA = 0, 1, 2, 3
+PKV_ERR_SCRATCH_TOO_SMALL = 4
 PKV_ERRF_BLOCK_ID, PKV_ERRF_SEQ_LEN, PKV_ERRF_SPLITS, PKV_ERRF_INDPTR, PKV_ERRF_TIMEOUT = (
     1, 2, 4, 8, 16)
 
@@ -101,6 +104,11 @@ def lib() -> ctypes.CDLL:
     L.compute_num_kv_splits.restype = ctypes.c_int
     L.compute_num_kv_splits.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                         _c_i32, _c_p]
+    L.paged_attention_v2_noalloc.restype = ctypes.c_int
+    L.paged_attention_v2_noalloc.argtypes = [_c_p, ctypes.POINTER(_c_i64), _c_i32, _c_i32, _c_p,
+                                             ctypes.POINTER(DecodeArgs), _c_p]
+    L.pkv_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    L.pkv_noalloc_scratch_bytes.argtypes = []
     if L.pkv_decode_args_size() != ctypes.sizeof(DecodeArgs):
         raise RuntimeError("pkv_decode_args_t layout mismatch between the library and the binding")
     _LIB = L
@@ -301,3 +309,35 @@ def compute_num_kv_splits(num_kv_splits: torch.Tensor, seq_lens: torch.Tensor, *
                                        int(num_head), int(num_kv_head), int(max_kv_splits),
                                        int(device_core_count), _stream(stream)),
            "compute_num_kv_splits")
+
+
+def noalloc_scratch_bytes() -> int:
+    """Size of the fixed device scratch array behind ``paged_attention_v2_noalloc``."""
+    return int(lib().pkv_noalloc_scratch_bytes())
+
+
+def paged_attention_v2_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                               value_cache: torch.Tensor, block_tables: torch.Tensor,
+                               seq_lens: torch.Tensor, scale: float, *, max_num_partitions: int,
+                               partition_size: int = 512,
+                               num_kv_splits: Optional[torch.Tensor] = None,
+                               kv_indptr: Optional[torch.Tensor] = None,
+                               err_flag: Optional[torch.Tensor] = None,
+                               max_blocks_per_seq: Optional[int] = None, stream=None) -> None:
+    """Split-KV decode into ``out`` for callers that cannot allocate device
+    memory: the partition scratch lives in the library's fixed device array
+    (see ``noalloc_scratch_bytes``) instead of caller-provided buffers.  Calls
+    share that array, so calls that overlap on the GPU race."""
+    _cuda(out, "out")
+    _cuda(num_kv_splits, "num_kv_splits")
+    if out.dtype != query.dtype or tuple(out.shape) != tuple(query.shape):
+        raise ValueError("out must match query's shape and dtype")
+    if num_kv_splits is not None and num_kv_splits.dtype != torch.int32:
+        raise ValueError("num_kv_splits must be int32")
+    a = _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
+                     err_flag, max_blocks_per_seq)
+    os_ = _I64x3(*out.stride())
+    _check(lib().paged_attention_v2_noalloc(_ptr(out), os_, int(max_num_partitions),
+                                            int(partition_size), _ptr(num_kv_splits),
+                                            ctypes.byref(a), _stream(stream)),
+           "paged_attention_v2_noalloc")

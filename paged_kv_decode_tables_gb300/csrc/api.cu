@@ -135,6 +135,7 @@ const char *pkv_status_string(pkv_status_t s) {
     case PKV_ERR_INVALID_ARG: return "invalid argument";
     case PKV_ERR_UNSUPPORTED: return "unsupported shape, dtype or layout";
     case PKV_ERR_CUDA: return "CUDA launch error";
+    case PKV_ERR_SCRATCH_TOO_SMALL: return "request exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }
