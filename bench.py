@@ -225,41 +225,63 @@ class DecodeStep:
         if st != 0:
             raise RuntimeError(f"{what} failed with status {st}")
 
-    def run(self, attn_events=None):
-        """Enqueue one step on the current stream; optionally record events
-        around the attention kernel."""
-        lib, pkv = self.lib, self.pkv
+    def run(self, attn_events=None, kernel_events=None):
+        """Enqueue one step on the current stream.  ``attn_events`` (a pair)
+        brackets the attention kernel; ``kernel_events`` (a dict of lists of
+        event pairs keyed by kernel) brackets every launch."""
+        lib = self.lib
         s = torch.cuda.current_stream().cuda_stream
+
+        def mark(name, i):
+            if kernel_events is not None:
+                kernel_events[name][-1][i].record()
+
+        def begin(name):
+            if kernel_events is not None:
+                kernel_events.setdefault(name, []).append(
+                    (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                mark(name, 0)
+
         if self.mode == "v2_splits":
             inp = self.inp
             bt = inp["block_tables"]
+            begin("copy_page_indices")
             self._check(lib.copy_page_indices(self.page_indices.data_ptr(), self.page_indices.numel(),
                                               bt.data_ptr(), bt.shape[1], bt.stride(0), bt.stride(1),
                                               self.cu.data_ptr(), self.B, None, s), "copy")
+            mark("copy_page_indices", 1)
             sp = self.spec
+            begin("compute_num_kv_splits")
             self._check(lib.compute_num_kv_splits(self.splits.data_ptr(), inp["seq_lens"].data_ptr(),
                                                   self.B, 1, self.H, self.Hk, sp.max_kv_splits,
                                                   sp.device_core_count, s), "splits")
+            mark("compute_num_kv_splits", 1)
         if attn_events is not None:
             attn_events[0].record()
         if self.mode == "v1":
+            begin("paged_attention_decode")
             self._check(lib.paged_attention_decode(self.out.data_ptr(), self.out_stride,
                                                    self.args_ref, s), "decode")
+            mark("paged_attention_decode", 1)
         else:
             splits = self.splits.data_ptr() if self.mode == "v2_splits" else None
             P = 0 if self.mode == "v2_splits" else self.spec.partition_size
+            begin("paged_attention_v2_partition")
             self._check(lib.paged_attention_v2_partition(self.tmp.data_ptr(), self.es.data_ptr(),
                                                          self.ml.data_ptr(), self.maxP, P, splits,
                                                          self.args_ref, s), "partition")
+            mark("paged_attention_v2_partition", 1)
         if attn_events is not None:
             attn_events[1].record()
         if self.mode != "v1":
             splits = self.splits.data_ptr() if self.mode == "v2_splits" else None
+            begin("paged_attention_v2_reduce")
             self._check(lib.paged_attention_v2_reduce(
                 self.out.data_ptr(), self.out_stride, self.tmp.data_ptr(), self.es.data_ptr(),
                 self.ml.data_ptr(), self.inp["seq_lens"].data_ptr(), splits, self.B, self.H,
                 self.D, self.bs, self.maxP, self.spec.partition_size, self.args.dtype, None, s),
                 "reduce")
+            mark("paged_attention_v2_reduce", 1)
 
     def host_inputs(self):
         """Pinned host copies of the per-step inputs (query, lengths, table,
@@ -496,6 +518,15 @@ def run_ours(args):
 
     elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
 
+    # per-kernel breakdown over a separate run of steps (events around every launch)
+    kev = {}
+    nb = min(K, 200)
+    for _ in range(nb):
+        step.run(kernel_events=kev)
+    torch.cuda.synchronize()
+    kernel_us = {k: round(sum(a.elapsed_time(b) for a, b in v) / len(v) * 1e3, 2)
+                 for k, v in kev.items()}
+
     # end to end through host buffers (per step: H2D of the inputs, the step,
     # D2H of the output, host waits for it)
     hin, hout = step.host_inputs()
@@ -568,6 +599,7 @@ def run_ours(args):
                                   round(attn_sorted[(9 * len(attn_sorted)) // 10] * 1e3, 2)],
         },
         "step_share": {"attention_kernel": round(attn_avg_ms / ms_step, 4)},
+        "kernel_us": kernel_us,
         "e2e": {"value": round(aggregate_gbs(step.kv_bytes, world, e2e_s / Ke), 2), "unit": UNIT,
                 "us_per_step": round(e2e_s / Ke * 1e6, 2), "steps": Ke,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -6,8 +6,8 @@
 // maximum goes round by shuffles; partitions are then taken 32 at a time:
 // each lane computes one partition's weight, the weights are broadcast by
 // shuffle and every lane accumulates its slice of the fp32 partial rows (one
-// coalesced row read per partition).  Up to 32 partitions: one warp per
-// (sequence, head), eight per CTA, no shared memory.  More: one CTA per
+// coalesced row read per partition).  Up to 32 partitions: each warp takes
+// two (sequence, head) pairs, no shared memory.  More: one CTA per
 // (sequence, head) whose eight warps take the groups of 32 in turn and add up
 // in shared memory.  No host sync and no inter-CTA waiting either way.
 #include "reduce.cuh"
@@ -56,10 +56,10 @@ struct Row<8> {
   }
 };
 
-// Non-empty partitions of sequence s, computed exactly as the partition
-// pass splits it (fixed size, or roundup(cdiv(L, n), block_size) tokens).
-__device__ __forceinline__ int count_parts(const ReduceParams &p, int s, bool report) {
-  int L = p.seq_lens[s];
+// Non-empty partitions of a sequence of length L (split count n, when the
+// split mode is on), computed exactly as the partition pass splits it: fixed
+// size, or roundup(cdiv(L, n), block_size) tokens.
+__device__ __forceinline__ int count_parts(const ReduceParams &p, int L, int n, bool report) {
   if (L < 0) {
     if (report) flag_error(p.err, 2u);
     L = 0;
@@ -68,7 +68,6 @@ __device__ __forceinline__ int count_parts(const ReduceParams &p, int s, bool re
   if (p.splits == nullptr) {
     num_parts = int((int64_t(L) + p.partition_size - 1) / p.partition_size);
   } else {
-    int n = p.splits[s];
     if (L > 0 && (n < 1 || n > p.max_parts)) {
       if (report) flag_error(p.err, 4u);
       n = n < 1 ? 1 : p.max_parts;
@@ -116,48 +115,62 @@ __device__ __forceinline__ void accumulate_parts(const float *ml, const float *e
   }
 }
 
-// One warp per (sequence, head): for up to a few dozen partitions.
+// Two (sequence, head) units per warp: for up to a few dozen partitions.
+// Every load that does not depend on another (length, split count and the
+// first partial row, which is the whole answer for a one-partition sequence)
+// is issued before any result is used.
+constexpr int kUnitsPerWarp = 2;
+
 template <typename TO, int D>
 __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p) {
   constexpr int V = D / 32;
+  constexpr int U = kUnitsPerWarp;
   const int lane = threadIdx.x & 31;
-  const int64_t unit = int64_t(blockIdx.x) * kReduceWarps + (threadIdx.x >> 5);
-  if (unit >= int64_t(p.num_seqs) * p.num_heads) return;
-  const int s = int(unit / p.num_heads);
-  const int h = int(unit % p.num_heads);
-  const int num_parts = count_parts(p, s, lane == 0);
-  TO *out = static_cast<TO *>(p.out) + int64_t(s) * p.o_s0 + int64_t(h) * p.o_s1;
-  const int64_t row = unit * p.max_parts;  // == (s * num_heads + h) * max_parts
-  const float *tmp = p.tmp + row * D + lane * V;
-  if (num_parts <= 1) {
-    // One partition is already normalised: the output is its row.
-    float v[V];
-    if (num_parts == 1) {
-      Row<V>::load(tmp, v);
-    } else {
+  const int64_t total = int64_t(p.num_seqs) * p.num_heads;
+  const int64_t first = (int64_t(blockIdx.x) * kReduceWarps + (threadIdx.x >> 5)) * U;
+  int Ls[U], ns[U];
+  float row0[U][V];
 #pragma unroll
-      for (int k = 0; k < V; ++k) v[k] = 0.f;
-    }
-#pragma unroll
-    for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(v[k]);
-    return;
+  for (int u = 0; u < U; ++u) {
+    const int64_t unit = min(first + u, total - 1);
+    const int s = int(unit / p.num_heads);
+    Ls[u] = __ldg(p.seq_lens + s);
+    ns[u] = p.splits != nullptr ? __ldg(p.splits + s) : 0;
+    Row<V>::load(p.tmp + unit * p.max_parts * D + lane * V, row0[u]);
   }
-  const float *ml = p.ml + row;
-  const float *es = p.es + row;
-  float M = -INFINITY;
-  for (int i = lane; i < num_parts; i += 32) M = fmaxf(M, __ldg(ml + i));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-  float S = 0.f;
-  float acc[V];
+  for (int u = 0; u < U; ++u) {
+    const int64_t unit = first + u;
+    if (unit >= total) break;
+    const int s = int(unit / p.num_heads);
+    const int h = int(unit % p.num_heads);
+    const int num_parts = count_parts(p, Ls[u], ns[u], lane == 0);
+    TO *out = static_cast<TO *>(p.out) + int64_t(s) * p.o_s0 + int64_t(h) * p.o_s1;
+    if (num_parts <= 1) {
+      // One partition is already normalised: the output is its row.
 #pragma unroll
-  for (int k = 0; k < V; ++k) acc[k] = 0.f;
-  accumulate_parts<D>(ml, es, tmp, num_parts, M, 0, 32, acc, S);
+      for (int k = 0; k < V; ++k)
+        out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(num_parts == 1 ? row0[u][k] : 0.f);
+      continue;
+    }
+    const int64_t row = unit * p.max_parts;  // == (s * num_heads + h) * max_parts
+    const float *ml = p.ml + row;
+    const float *es = p.es + row;
+    float M = -INFINITY;
+    for (int i = lane; i < num_parts; i += 32) M = fmaxf(M, __ldg(ml + i));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
-  const float inv = __fdiv_rn(1.f, S);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float S = 0.f;
+    float acc[V];
 #pragma unroll
-  for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(acc[k] * inv);
+    for (int k = 0; k < V; ++k) acc[k] = 0.f;
+    accumulate_parts<D>(ml, es, p.tmp + row * D + lane * V, num_parts, M, 0, 32, acc, S);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+    const float inv = __fdiv_rn(1.f, S);
+#pragma unroll
+    for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(acc[k] * inv);
+  }
 }
 
 // One CTA per (sequence, head), the eight warps taking groups of 32
@@ -172,7 +185,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_wide_kernel(const Re
   const int64_t unit = blockIdx.x;
   const int s = int(unit / p.num_heads);
   const int h = int(unit % p.num_heads);
-  const int num_parts = count_parts(p, s, threadIdx.x == 0);
+  const int num_parts = count_parts(p, p.seq_lens[s], p.splits != nullptr ? p.splits[s] : 0,
+                                    threadIdx.x == 0);
   TO *out = static_cast<TO *>(p.out) + int64_t(s) * p.o_s0 + int64_t(h) * p.o_s1;
   if (num_parts == 0) {
     for (int d = threadIdx.x; d < D; d += kReduceWarps * 32) out[int64_t(d) * p.o_s2] = from_f32<TO>(0.f);
@@ -220,7 +234,8 @@ pkv_status_t launch_d(const ReduceParams &p, cudaStream_t stream) {
     if (units > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     reduce_wide_kernel<TO, D><<<unsigned(units), kReduceWarps * 32, 0, stream>>>(p);
   } else {
-    const int64_t blocks = (units + kReduceWarps - 1) / kReduceWarps;
+    const int64_t per_block = int64_t(kReduceWarps) * kUnitsPerWarp;
+    const int64_t blocks = (units + per_block - 1) / per_block;
     if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     reduce_kernel<TO, D><<<unsigned(blocks), kReduceWarps * 32, 0, stream>>>(p);
   }
