@@ -4,10 +4,12 @@
 One *step* is one pass of the whole decode path over one synthetic batch:
 for the ragged serving batch (the default workload) that is
 
-    copy_page_indices -> compute_num_kv_splits -> paged_attention_v2_partition
+    prepare_decode_metadata (copy_page_indices + compute_num_kv_splits in one
+    launch; --metadata separate launches the two) -> paged_attention_v2_partition
     (reading block ids through the flat page list) -> paged_attention_v2_reduce
 
-all launched through the C ABI on one stream.  The KV cache is resident
+all launched through the C ABI on one stream, captured once as a CUDA graph
+and replayed (--no-graph: plain stream launches).  The KV cache is resident
 device state (as in serving); inputs are larger than L2, so no flush is
 needed between steps (the tiny workload, which fits in L2, is flushed).
 
@@ -160,7 +162,7 @@ class DecodeStep:
     """Device buffers of one workload and the launches of one step, issued
     straight through the C ABI with argument structs prepared once."""
 
-    def __init__(self, name: str, seed: int, device, num_seqs=None):
+    def __init__(self, name: str, seed: int, device, num_seqs=None, fused_metadata=True):
         import ctypes
 
         import paged_kv_decode_tables_gb300 as pkv
@@ -213,7 +215,9 @@ class DecodeStep:
         self.args = pkv._decode_args(q, kc, vc, bt_for_attn, inp["seq_lens"], inp["scale"], indptr,
                                      None, None)
         self.args_ref = ctypes.byref(self.args)
-        self.launches_per_step = {"v1": 1, "v2_fixed": 2, "v2_splits": 4}[self.mode]
+        self.fused_metadata = fused_metadata
+        self.launches_per_step = {"v1": 1, "v2_fixed": 2,
+                                  "v2_splits": 3 if fused_metadata else 4}[self.mode]
         # Algorithmic bytes of one launch of the attention kernel: K+V of every
         # token, the queries, the block ids and lengths it reads, and (single
         # pass) its output.  The fp32 split-KV partials are counted apart.
@@ -242,7 +246,18 @@ class DecodeStep:
                     (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
                 mark(name, 0)
 
-        if self.mode == "v2_splits":
+        if self.mode == "v2_splits" and self.fused_metadata:
+            inp = self.inp
+            bt = inp["block_tables"]
+            sp = self.spec
+            begin("prepare_decode_metadata")
+            self._check(lib.prepare_decode_metadata(
+                self.page_indices.data_ptr(), self.page_indices.numel(), bt.data_ptr(), bt.shape[1],
+                bt.stride(0), bt.stride(1), self.cu.data_ptr(), self.B, self.splits.data_ptr(),
+                inp["seq_lens"].data_ptr(), 1, self.H, self.Hk, sp.max_kv_splits,
+                sp.device_core_count, None, s), "metadata")
+            mark("prepare_decode_metadata", 1)
+        elif self.mode == "v2_splits":
             inp = self.inp
             bt = inp["block_tables"]
             begin("copy_page_indices")
@@ -471,7 +486,8 @@ def run_ours(args):
         _build.build()
     if dist is not None:
         dist.barrier()
-    step = DecodeStep(args.workload, seed=rank, device="cuda", num_seqs=args.num_seqs)
+    step = DecodeStep(args.workload, seed=rank, device="cuda", num_seqs=args.num_seqs,
+                      fused_metadata=args.metadata == "fused")
     if args.warps:
         step.pkv.set_attention_warps(args.warps)
     spec = step.spec
@@ -483,6 +499,22 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
+    graph = None
+    if args.graph:
+        # one step captured as a CUDA graph and replayed (no per-launch events
+        # inside it; the attention kernel is then timed by the per-kernel pass)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                step.run()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step.run()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
     attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
     clocks = ClockSampler(torch.cuda.current_device()) if (rank == 0 and not args.no_clocks) else None
@@ -506,15 +538,19 @@ def run_ours(args):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record()
-        for i in range(K):
-            step.run(attn_ev[i])
+        if graph is not None:
+            for i in range(K):
+                graph.replay()
+        else:
+            for i in range(K):
+                step.run(attn_ev[i])
         t_end.record()
         torch.cuda.synchronize()
         elapsed_ms = t_start.elapsed_time(t_end)
     if dist is not None:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    attn_ms = None if graph is not None else [a.elapsed_time(b) for a, b in attn_ev]
 
     elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
 
@@ -526,6 +562,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     kernel_us = {k: round(sum(a.elapsed_time(b) for a, b in v) / len(v) * 1e3, 2)
                  for k, v in kev.items()}
+    if attn_ms is None:
+        attn_key = "paged_attention_decode" if step.mode == "v1" else "paged_attention_v2_partition"
+        attn_ms = [a.elapsed_time(b) for a, b in kev[attn_key]]
 
     # end to end through host buffers (per step: H2D of the inputs, the step,
     # D2H of the output, host waits for it)
@@ -583,6 +622,10 @@ def run_ours(args):
             "l2": ("flushed between steps (512 MB write)" if flush else
                    f"inputs larger than L2: {step.kv_bytes / 1e9:.2f} GB of K/V per step"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "launch": ("CUDA graph replay of the step" if graph is not None else
+                       "stream launches, programmatic dependent launch"),
+            "metadata": ("one launch (prepare_decode_metadata)" if step.fused_metadata else
+                         "copy_page_indices + compute_num_kv_splits") if step.mode == "v2_splits" else None,
         },
         "roofline": {
             "kernel": kern,
@@ -625,6 +668,10 @@ def main(argv=None):
                     help="smaller batch of the same workload (profiling captures only)")
     ap.add_argument("--warps", type=int, default=0, choices=[0, 1, 2, 4],
                     help="force warps per attention CTA (0: library default)")
+    ap.add_argument("--metadata", choices=["fused", "separate"], default="fused",
+                    help="ragged step: metadata in one launch or the two separate kernels")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time stream launches instead of CUDA-graph replays of the step")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

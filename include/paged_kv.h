@@ -243,6 +243,26 @@ pkv_status_t compute_num_kv_splits(int32_t *num_kv_splits, const int32_t *seq_le
                                    pkv_stream_t stream);
 
 /*
+ * Both metadata steps in one launch: exactly copy_page_indices(page_indices,
+ * page_indices_capacity, block_table, num_cols, bt_stride0, bt_stride1,
+ * cu_num_blocks, num_reqs, err_flag) followed by
+ * compute_num_kv_splits(num_kv_splits, seq_lens, num_reqs, num_group, num_head,
+ * num_kv_head, max_kv_splits, device_core_count), with the same arguments,
+ * outputs and errors (one sequence per request row).  The split heuristic runs
+ * on one CTA while the others copy table rows (a warp per row), so the decode
+ * step's metadata costs a single launch and no host sync (vLLM PR 35765 and
+ * sglang's get_num_kv_splits_triton are separate kernels on their pages).
+ */
+pkv_status_t prepare_decode_metadata(int32_t *page_indices, int64_t page_indices_capacity,
+                                     const int32_t *block_table, int32_t num_cols,
+                                     int64_t bt_stride0, int64_t bt_stride1,
+                                     const int32_t *cu_num_blocks, int32_t num_reqs,
+                                     int32_t *num_kv_splits, const int32_t *seq_lens,
+                                     int32_t num_group, int32_t num_head, int32_t num_kv_head,
+                                     int32_t max_kv_splits, int32_t device_core_count,
+                                     int32_t *err_flag, pkv_stream_t stream);
+
+/*
  * Split-KV decode (partition pass + reduce) that allocates nothing.
  *
  * The pages have no counterpart of this entry point; it exists for callers

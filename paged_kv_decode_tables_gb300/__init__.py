@@ -29,6 +29,7 @@ __all__ = [
     "paged_attention_v2_reduce",
     "copy_page_indices",
     "compute_num_kv_splits",
+    "prepare_decode_metadata",
     "paged_attention_v2_noalloc",
     "noalloc_scratch_bytes",
 ]
@@ -104,6 +105,10 @@ def lib() -> ctypes.CDLL:
     L.compute_num_kv_splits.restype = ctypes.c_int
     L.compute_num_kv_splits.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                         _c_i32, _c_p]
+    L.prepare_decode_metadata.restype = ctypes.c_int
+    L.prepare_decode_metadata.argtypes = [_c_p, _c_i64, _c_p, _c_i32, _c_i64, _c_i64, _c_p, _c_i32,
+                                          _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p,
+                                          _c_p]
     L.paged_attention_v2_noalloc.restype = ctypes.c_int
     L.paged_attention_v2_noalloc.argtypes = [_c_p, ctypes.POINTER(_c_i64), _c_i32, _c_i32, _c_p,
                                              ctypes.POINTER(DecodeArgs), _c_p]
@@ -309,6 +314,37 @@ def compute_num_kv_splits(num_kv_splits: torch.Tensor, seq_lens: torch.Tensor, *
                                        int(num_head), int(num_kv_head), int(max_kv_splits),
                                        int(device_core_count), _stream(stream)),
            "compute_num_kv_splits")
+
+
+def prepare_decode_metadata(page_indices: torch.Tensor, block_table: torch.Tensor,
+                            cu_num_blocks: torch.Tensor, num_kv_splits: torch.Tensor,
+                            seq_lens: torch.Tensor, *, num_group: int, num_head: int,
+                            num_kv_head: int, max_kv_splits: int, device_core_count: int,
+                            err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """``copy_page_indices`` and ``compute_num_kv_splits`` in one launch."""
+    for t, n in ((page_indices, "page_indices"), (block_table, "block_table"),
+                 (cu_num_blocks, "cu_num_blocks"), (num_kv_splits, "num_kv_splits"),
+                 (seq_lens, "seq_lens"), (err_flag, "err_flag")):
+        _cuda(t, n)
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    if block_table.dim() != 2 or cu_num_blocks.dim() != 1 or page_indices.dim() != 1:
+        raise ValueError("expected block_table [R, C], cu_num_blocks [R+1], page_indices [N]")
+    for t, n in ((page_indices, "page_indices"), (cu_num_blocks, "cu_num_blocks"),
+                 (num_kv_splits, "num_kv_splits"), (seq_lens, "seq_lens")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    R = cu_num_blocks.shape[0] - 1
+    if R > block_table.shape[0] or seq_lens.numel() != R or num_kv_splits.numel() < R * num_group:
+        raise ValueError("inconsistent row counts")
+    s0, s1 = block_table.stride()
+    _check(lib().prepare_decode_metadata(_ptr(page_indices), page_indices.numel(),
+                                         _ptr(block_table), block_table.shape[1], s0, s1,
+                                         _ptr(cu_num_blocks), R, _ptr(num_kv_splits),
+                                         _ptr(seq_lens), int(num_group), int(num_head),
+                                         int(num_kv_head), int(max_kv_splits),
+                                         int(device_core_count), _ptr(err_flag), _stream(stream)),
+           "prepare_decode_metadata")
 
 
 def noalloc_scratch_bytes() -> int:

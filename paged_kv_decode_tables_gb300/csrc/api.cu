@@ -261,6 +261,27 @@ pkv_status_t compute_num_kv_splits(int32_t *num_kv_splits, const int32_t *seq_le
                                    reinterpret_cast<cudaStream_t>(stream));
 }
 
+pkv_status_t prepare_decode_metadata(int32_t *page_indices, int64_t page_indices_capacity,
+                                     const int32_t *block_table, int32_t num_cols,
+                                     int64_t bt_stride0, int64_t bt_stride1,
+                                     const int32_t *cu_num_blocks, int32_t num_reqs,
+                                     int32_t *num_kv_splits, const int32_t *seq_lens,
+                                     int32_t num_group, int32_t num_head, int32_t num_kv_head,
+                                     int32_t max_kv_splits, int32_t device_core_count,
+                                     int32_t *err_flag, pkv_stream_t stream) {
+  if (num_reqs < 1 || num_cols < 0 || page_indices_capacity < 0) return PKV_ERR_INVALID_ARG;
+  if (!page_indices || !block_table || !cu_num_blocks || !num_kv_splits || !seq_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (num_group < 1 || num_head < 1 || num_kv_head < 1 || num_head < num_kv_head ||
+      max_kv_splits < 1 || device_core_count < 1)
+    return PKV_ERR_INVALID_ARG;
+  return pkv::launch_decode_metadata(page_indices, page_indices_capacity, block_table, num_cols,
+                                     bt_stride0, bt_stride1, cu_num_blocks, num_reqs,
+                                     num_kv_splits, seq_lens, num_group, num_head, num_kv_head,
+                                     max_kv_splits, device_core_count, err_flag,
+                                     reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"
 
 namespace pkv {

@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int lane = threadIdx.x & 31;
   const int g = p.group;
   const bool leader = threadIdx.x == 0;
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   // ---------------------------------------------------- work decomposition --
   int L = p.seq_lens[seq];
@@ -149,11 +151,9 @@ __global__ void __launch_bounds__(WARPS * 32)
       if (leader) flag_error(p.err, 4u);
       n = clamp_int(n, 1, p.max_parts);
     }
+    // chunk = roundup(cdiv(L, n), BS); 32-bit is exact since 0 < L < 2^31
     int64_t c = BS;
-    if (L > 0 && n > 0) {
-      c = (int64_t(L) + n - 1) / n;
-      c = (c + BS - 1) / BS * BS;
-    }
+    if (L > 0 && n > 0) c = ((unsigned(L) - 1u) / unsigned(n) + BS) / BS * BS;
     t0 = int64_t(part) * c;
     t1 = part < n ? min(t0 + c, int64_t(L)) : t0;
   }

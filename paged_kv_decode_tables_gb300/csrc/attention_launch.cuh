@@ -7,6 +7,7 @@
 
 #include "../../include/paged_kv.h"
 #include "attention_kernel.cuh"
+#include "pkv_launch.cuh"
 
 namespace pkv {
 
@@ -41,8 +42,10 @@ pkv_status_t launch_instance(const AttnParams &p, dim3 grid, cudaStream_t stream
   static std::atomic<unsigned long long> done{0};
   auto kernel = paged_attention_kernel<T, D, BS, W>;
   if (!ensure_smem_attr(kernel, Cfg::kSmemBytes, done)) return PKV_ERR_CUDA;
-  kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return launch_programmatic(kernel, grid, dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) ==
+                 cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }
 
 // Instances are built for WARPS in {1, 2, 4}; a 4-warp instance only when its

@@ -7,7 +7,10 @@
 // compute_num_kv_splits: sglang metadata.py, get_num_kv_splits_triton.  One
 //   CTA: block-wide max/min of the lengths, the split formula evaluated once,
 //   then every thread writes its sequences' counts.
+// prepare_decode_metadata: both of the above in one launch (a warp per table
+//   row, plus one CTA for the split counts).
 #include "metadata.cuh"
+#include "pkv_launch.cuh"
 
 namespace pkv {
 
@@ -15,40 +18,44 @@ namespace {
 
 constexpr int kCopyThreads = 128;
 constexpr int kSplitThreads = 1024;
+constexpr int kFusedThreads = 256;  // fused launch: a warp per table row, one CTA for the splits
 
-__global__ void __launch_bounds__(kCopyThreads)
-    copy_page_indices_kernel(int32_t *__restrict__ out, int64_t capacity,
-                             const int32_t *__restrict__ bt, int32_t num_cols, int64_t s0,
-                             int64_t s1, const int32_t *__restrict__ cu, int32_t *err) {
-  const int i = blockIdx.x;
+__device__ __forceinline__ int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Row i of the page-index copy, its columns shared by `nthreads` threads
+// starting at `tid`.
+__device__ __forceinline__ void copy_row(int32_t *__restrict__ out, int64_t capacity,
+                                         const int32_t *__restrict__ bt, int32_t num_cols,
+                                         int64_t s0, int64_t s1, const int32_t *__restrict__ cu,
+                                         int32_t *err, int i, int tid, int nthreads) {
   const int64_t start = cu[i];
   int64_t n = int64_t(cu[i + 1]) - start;
   if (start < 0 || n < 0 || n > num_cols) {
-    if (threadIdx.x == 0) flag_error(err, 8u);
+    if (tid == 0) flag_error(err, 8u);
     if (start < 0) return;
     n = n < 0 ? 0 : num_cols;
   }
   if (start + n > capacity) {
-    if (threadIdx.x == 0) flag_error(err, 8u);
+    if (tid == 0) flag_error(err, 8u);
     n = capacity > start ? capacity - start : 0;
   }
   const int32_t *row = bt + int64_t(i) * s0;
   int32_t *dst = out + start;
-  for (int64_t j = threadIdx.x; j < n; j += kCopyThreads) dst[j] = __ldg(row + j * s1);
+  for (int64_t j = tid; j < n; j += nthreads) dst[j] = __ldg(row + j * s1);
 }
 
-__device__ __forceinline__ int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-__global__ void __launch_bounds__(kSplitThreads)
-    num_kv_splits_kernel(int32_t *__restrict__ out, const int32_t *__restrict__ seq_lens,
-                         int32_t num_seq, int32_t num_group, int32_t num_head,
-                         int32_t num_kv_head, int32_t max_kv_splits, int32_t core_count) {
-  __shared__ int red_max[kSplitThreads / 32], red_min[kSplitThreads / 32];
+// The split-count heuristic on one CTA of THREADS threads.
+template <int THREADS>
+__device__ __forceinline__ void split_counts(int32_t *__restrict__ out,
+                                             const int32_t *__restrict__ seq_lens, int32_t num_seq,
+                                             int32_t num_group, int32_t num_head,
+                                             int32_t num_kv_head, int32_t max_kv_splits,
+                                             int32_t core_count) {
+  __shared__ int red_max[THREADS / 32], red_min[THREADS / 32];
   __shared__ int64_t chunk[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
   int mx = 1, mn = 0x7fffffff;
-  for (int s = tid; s < num_seq; s += kSplitThreads) {
+  for (int s = tid; s < num_seq; s += THREADS) {
     const int L = max(seq_lens[s], 1);
     mx = max(mx, L);
     mn = min(mn, L);
@@ -64,7 +71,7 @@ __global__ void __launch_bounds__(kSplitThreads)
   }
   __syncthreads();
   if (tid == 0) {
-    for (int w = 1; w < kSplitThreads / 32; ++w) {
+    for (int w = 1; w < THREADS / 32; ++w) {
       mx = max(mx, red_max[w]);
       mn = min(mn, red_min[w]);
     }
@@ -93,11 +100,51 @@ __global__ void __launch_bounds__(kSplitThreads)
   }
   __syncthreads();
   const int64_t c1 = chunk[0], c2 = chunk[1];
-  for (int s = tid; s < num_seq; s += kSplitThreads) {
+  for (int s = tid; s < num_seq; s += THREADS) {
     const int64_t L = max(seq_lens[s], 0);
     const int v = int(max(cdiv64(L, c1), cdiv64(L, c2)));
     for (int i = 0; i < num_group; ++i) out[int64_t(s) * num_group + i] = v;
   }
+}
+
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_page_indices_kernel(int32_t *__restrict__ out, int64_t capacity,
+                             const int32_t *__restrict__ bt, int32_t num_cols, int64_t s0,
+                             int64_t s1, const int32_t *__restrict__ cu, int32_t *err) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  copy_row(out, capacity, bt, num_cols, s0, s1, cu, err, blockIdx.x, threadIdx.x, kCopyThreads);
+}
+
+__global__ void __launch_bounds__(kSplitThreads)
+    num_kv_splits_kernel(int32_t *__restrict__ out, const int32_t *__restrict__ seq_lens,
+                         int32_t num_seq, int32_t num_group, int32_t num_head,
+                         int32_t num_kv_head, int32_t max_kv_splits, int32_t core_count) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  split_counts<kSplitThreads>(out, seq_lens, num_seq, num_group, num_head, num_kv_head,
+                              max_kv_splits, core_count);
+}
+
+// Both metadata steps in one grid: blocks [0, copy_blocks) copy table rows (a
+// warp per row), the last block computes the split counts.
+__global__ void __launch_bounds__(kFusedThreads)
+    decode_metadata_kernel(int32_t *__restrict__ page_indices, int64_t capacity,
+                           const int32_t *__restrict__ bt, int32_t num_cols, int64_t s0,
+                           int64_t s1, const int32_t *__restrict__ cu, int32_t num_reqs,
+                           int32_t *__restrict__ splits, const int32_t *__restrict__ seq_lens,
+                           int32_t num_group, int32_t num_head, int32_t num_kv_head,
+                           int32_t max_kv_splits, int32_t core_count, int32_t *err) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  if (blockIdx.x == gridDim.x - 1) {
+    split_counts<kFusedThreads>(splits, seq_lens, num_reqs, num_group, num_head, num_kv_head,
+                                max_kv_splits, core_count);
+    return;
+  }
+  const int row = blockIdx.x * (kFusedThreads / 32) + (threadIdx.x >> 5);
+  if (row < num_reqs)
+    copy_row(page_indices, capacity, bt, num_cols, s0, s1, cu, err, row, threadIdx.x & 31, 32);
 }
 
 }  // namespace
@@ -107,20 +154,38 @@ pkv_status_t launch_copy_page_indices(int32_t *page_indices, int64_t capacity,
                                       int64_t s1, const int32_t *cu, int32_t num_reqs,
                                       int32_t *err, cudaStream_t stream) {
   if (num_reqs == 0) return PKV_OK;
-  copy_page_indices_kernel<<<num_reqs, kCopyThreads, 0, stream>>>(page_indices, capacity,
-                                                                 block_table, num_cols, s0, s1,
-                                                                 cu, err);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return launch_programmatic(copy_page_indices_kernel, dim3(num_reqs), dim3(kCopyThreads), 0,
+                             stream, page_indices, capacity, block_table, num_cols, s0, s1, cu,
+                             err) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }
 
 pkv_status_t launch_num_kv_splits(int32_t *out, const int32_t *seq_lens, int32_t num_seq,
                                   int32_t num_group, int32_t num_head, int32_t num_kv_head,
                                   int32_t max_kv_splits, int32_t core_count,
                                   cudaStream_t stream) {
-  num_kv_splits_kernel<<<1, kSplitThreads, 0, stream>>>(out, seq_lens, num_seq, num_group,
-                                                        num_head, num_kv_head, max_kv_splits,
-                                                        core_count);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return launch_programmatic(num_kv_splits_kernel, dim3(1), dim3(kSplitThreads), 0, stream, out,
+                             seq_lens, num_seq, num_group, num_head, num_kv_head, max_kv_splits,
+                             core_count) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+pkv_status_t launch_decode_metadata(int32_t *page_indices, int64_t capacity,
+                                    const int32_t *block_table, int32_t num_cols, int64_t s0,
+                                    int64_t s1, const int32_t *cu, int32_t num_reqs,
+                                    int32_t *splits, const int32_t *seq_lens, int32_t num_group,
+                                    int32_t num_head, int32_t num_kv_head, int32_t max_kv_splits,
+                                    int32_t core_count, int32_t *err, cudaStream_t stream) {
+  const int rows_per_block = kFusedThreads / 32;
+  const int copy_blocks = (num_reqs + rows_per_block - 1) / rows_per_block;
+  return launch_programmatic(decode_metadata_kernel, dim3(copy_blocks + 1), dim3(kFusedThreads), 0,
+                             stream, page_indices, capacity, block_table, num_cols, s0, s1, cu,
+                             num_reqs, splits, seq_lens, num_group, num_head, num_kv_head,
+                             max_kv_splits, core_count, err) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

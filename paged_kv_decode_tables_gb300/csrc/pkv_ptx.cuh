@@ -19,6 +19,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ------------------------------------------------ programmatic launch order --
+
+// Wait until the grid launched before this one on the stream has completed
+// and its memory is visible (a no-op when the launch was not programmatic).
+// Every kernel calls it before reading any input: a predecessor may write them.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid on the stream to be scheduled now; it still waits in
+// grid_dependency_wait() for this grid to finish.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

@@ -10,6 +10,7 @@
 // two (sequence, head) pairs, no shared memory.  More: one CTA per
 // (sequence, head) whose eight warps take the groups of 32 in turn and add up
 // in shared memory.  No host sync and no inter-CTA waiting either way.
+#include "pkv_launch.cuh"
 #include "reduce.cuh"
 
 namespace pkv {
@@ -65,20 +66,19 @@ __device__ __forceinline__ int count_parts(const ReduceParams &p, int L, int n, 
     L = 0;
   }
   int num_parts;
-  if (p.splits == nullptr) {
-    num_parts = int((int64_t(L) + p.partition_size - 1) / p.partition_size);
+  if (L == 0) {
+    num_parts = 0;
+  } else if (p.splits == nullptr) {
+    num_parts = int((unsigned(L) - 1u) / unsigned(p.partition_size)) + 1;
   } else {
-    if (L > 0 && (n < 1 || n > p.max_parts)) {
+    if (n < 1 || n > p.max_parts) {
       if (report) flag_error(p.err, 4u);
       n = n < 1 ? 1 : p.max_parts;
     }
-    if (L > 0) {
-      int64_t c = (int64_t(L) + n - 1) / n;
-      c = (c + p.block_size - 1) / p.block_size * p.block_size;
-      num_parts = int((L + c - 1) / c);
-    } else {
-      num_parts = 0;
-    }
+    // chunk = roundup(cdiv(L, n), block_size); 32-bit is exact since L < 2^31
+    const unsigned bs = unsigned(p.block_size);
+    const unsigned c = ((unsigned(L) - 1u) / unsigned(n) + bs) / bs * bs;
+    num_parts = int((unsigned(L) - 1u) / c) + 1;
   }
   if (num_parts > p.max_parts) {
     if (report) flag_error(p.err, 2u);
@@ -120,30 +120,35 @@ __device__ __forceinline__ void accumulate_parts(const float *ml, const float *e
 // first partial row, which is the whole answer for a one-partition sequence)
 // is issued before any result is used.
 constexpr int kUnitsPerWarp = 2;
+constexpr int kPrefetch = 8;  // partial rows fetched together with the statistics
 
 template <typename TO, int D>
 __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p) {
   constexpr int V = D / 32;
   constexpr int U = kUnitsPerWarp;
   const int lane = threadIdx.x & 31;
-  const int64_t total = int64_t(p.num_seqs) * p.num_heads;
-  const int64_t first = (int64_t(blockIdx.x) * kReduceWarps + (threadIdx.x >> 5)) * U;
+  // (sequence, head) units number below 2^31 (checked at launch): 32-bit math.
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const unsigned total = unsigned(p.num_seqs) * unsigned(p.num_heads);
+  const unsigned H = unsigned(p.num_heads);
+  const unsigned first = (blockIdx.x * kReduceWarps + (threadIdx.x >> 5)) * U;
   int Ls[U], ns[U];
   float row0[U][V];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const int64_t unit = min(first + u, total - 1);
-    const int s = int(unit / p.num_heads);
+    const unsigned unit = min(first + u, total - 1);
+    const int s = int(unit / H);
     Ls[u] = __ldg(p.seq_lens + s);
     ns[u] = p.splits != nullptr ? __ldg(p.splits + s) : 0;
-    Row<V>::load(p.tmp + unit * p.max_parts * D + lane * V, row0[u]);
+    Row<V>::load(p.tmp + int64_t(unit) * p.max_parts * D + lane * V, row0[u]);
   }
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const int64_t unit = first + u;
+    const unsigned unit = first + u;
     if (unit >= total) break;
-    const int s = int(unit / p.num_heads);
-    const int h = int(unit % p.num_heads);
+    const int s = int(unit / H);
+    const int h = int(unit - unsigned(s) * H);
     const int num_parts = count_parts(p, Ls[u], ns[u], lane == 0);
     TO *out = static_cast<TO *>(p.out) + int64_t(s) * p.o_s0 + int64_t(h) * p.o_s1;
     if (num_parts <= 1) {
@@ -153,20 +158,46 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
         out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(num_parts == 1 ? row0[u][k] : 0.f);
       continue;
     }
-    const int64_t row = unit * p.max_parts;  // == (s * num_heads + h) * max_parts
-    const float *ml = p.ml + row;
-    const float *es = p.es + row;
-    float M = -INFINITY;
-    for (int i = lane; i < num_parts; i += 32) M = fmaxf(M, __ldg(ml + i));
+    // At most 32 partitions here: lane i holds partition i's statistics, and
+    // the first kPrefetch partial rows are fetched in the same round.
+    const int64_t row = int64_t(unit) * p.max_parts;  // == (s * num_heads + h) * max_parts
+    const bool mine = lane < num_parts;
+    const float mlv = mine ? __ldg(p.ml + row + lane) : -INFINITY;
+    const float esv = mine ? __ldg(p.es + row + lane) : 0.f;
+    const float *tmp = p.tmp + row * D + lane * V;
+    float rows[kPrefetch][V];
+#pragma unroll
+    for (int j = 1; j < kPrefetch; ++j) {
+      if (j < num_parts) Row<V>::load(tmp + int64_t(j) * D, rows[j]);
+    }
+    float M = mlv;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    float S = 0.f;
-    float acc[V];
-#pragma unroll
-    for (int k = 0; k < V; ++k) acc[k] = 0.f;
-    accumulate_parts<D>(ml, es, p.tmp + row * D + lane * V, num_parts, M, 0, 32, acc, S);
+    const float w = mine ? ex2((mlv - M) * kLog2e) * esv : 0.f;
+    float S = w;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+    float acc[V];
+    {
+      const float w0 = __shfl_sync(kFull, w, 0);
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] = w0 * row0[u][k];
+    }
+#pragma unroll
+    for (int j = 1; j < kPrefetch; ++j) {
+      const float wj = __shfl_sync(kFull, w, j);
+      if (j < num_parts) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) acc[k] = fmaf(wj, rows[j][k], acc[k]);
+      }
+    }
+    for (int j = kPrefetch; j < num_parts; ++j) {
+      const float wj = __shfl_sync(kFull, w, j);
+      float v[V];
+      Row<V>::load(tmp + int64_t(j) * D, v);
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] = fmaf(wj, v[k], acc[k]);
+    }
     const float inv = __fdiv_rn(1.f, S);
 #pragma unroll
     for (int k = 0; k < V; ++k) out[int64_t(lane * V + k) * p.o_s2] = from_f32<TO>(acc[k] * inv);
@@ -182,6 +213,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_wide_kernel(const Re
   __shared__ float part_S[kReduceWarps];
   __shared__ __align__(16) float part_acc[kReduceWarps][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int64_t unit = blockIdx.x;
   const int s = int(unit / p.num_heads);
   const int h = int(unit % p.num_heads);
@@ -230,16 +263,21 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_wide_kernel(const Re
 template <typename TO, int D>
 pkv_status_t launch_d(const ReduceParams &p, cudaStream_t stream) {
   const int64_t units = int64_t(p.num_seqs) * p.num_heads;
+  if (units >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
   if (p.max_parts > 32) {
     if (units > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
-    reduce_wide_kernel<TO, D><<<unsigned(units), kReduceWarps * 32, 0, stream>>>(p);
+    if (launch_programmatic(reduce_wide_kernel<TO, D>, dim3(unsigned(units)),
+                            dim3(kReduceWarps * 32), 0, stream, p) != cudaSuccess)
+      return PKV_ERR_CUDA;
   } else {
     const int64_t per_block = int64_t(kReduceWarps) * kUnitsPerWarp;
     const int64_t blocks = (units + per_block - 1) / per_block;
     if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
-    reduce_kernel<TO, D><<<unsigned(blocks), kReduceWarps * 32, 0, stream>>>(p);
+    if (launch_programmatic(reduce_kernel<TO, D>, dim3(unsigned(blocks)), dim3(kReduceWarps * 32),
+                            0, stream, p) != cudaSuccess)
+      return PKV_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 template <typename TO>

@@ -150,6 +150,10 @@ def test_reduce_and_metadata_reject_bad_arguments(lib):
     assert lib.compute_num_kv_splits(p, p, 4, 1, 32, 8, 0, 148, None) == 1
     assert lib.compute_num_kv_splits(p, p, 4, 1, 32, 8, 16, 0, None) == 1
     assert lib.copy_page_indices(0, 10, p, 4, 4, 1, p, 2, None, None) == 1
+    assert lib.prepare_decode_metadata(p, 10, p, 4, 4, 1, p, 0, p, p, 1, 32, 8, 16, 148, None,
+                                       None) == 1
+    assert lib.prepare_decode_metadata(p, 10, p, 4, 4, 1, p, 2, p, p, 1, 8, 32, 16, 148, None,
+                                       None) == 1
     assert lib.pkv_set_attention_warps(3) == 1
     assert lib.pkv_set_attention_warps(0) == 0
 

@@ -119,3 +119,31 @@ def test_num_kv_splits_float32_step_exhaustive():
     got = out.cpu().tolist()
     bad = [(k // 2 + 1, got[k], want[k]) for k in range(2 * N) if got[k] != want[k]]
     assert not bad, bad[:10]
+
+
+@pytest.mark.parametrize("col_step", [1, 2])
+@pytest.mark.parametrize("R", [1, 7, 9, 512, 1000])
+def test_fused_metadata_equals_both_steps(R, col_step):
+    """prepare_decode_metadata == copy_page_indices + compute_num_kv_splits, bit for bit."""
+    g = torch.Generator().manual_seed(R + 17 * col_step)
+    W = 300
+    storage = torch.randint(0, 1 << 20, (R, W * col_step), generator=g, dtype=torch.int32)
+    bt = storage[:, ::col_step]
+    lens = torch.randint(0, W * 16 + 1, (R,), generator=g)
+    lens[0] = 1
+    n = [-(-int(L) // 16) for L in lens]
+    cu = [0]
+    for v in n:
+        cu.append(cu[-1] + v)
+    cap = cu[-1] + 5
+    pi = torch.full((cap,), -3, dtype=torch.int32, device="cuda")
+    splits = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.prepare_decode_metadata(pi, storage.cuda()[:, ::col_step],
+                                torch.tensor(cu, dtype=torch.int32, device="cuda"), splits,
+                                lens.to(torch.int32).cuda(), num_group=1, num_head=32,
+                                num_kv_head=8, max_kv_splits=16, device_core_count=148,
+                                err_flag=err)
+    assert pi.cpu().tolist() == oracle.copy_page_indices(bt, cu, cap, fill=-3)
+    assert splits.cpu().tolist() == oracle.num_kv_splits(lens.tolist(), 1, 32, 8, 16, 148)
+    assert int(err.item()) == 0
