@@ -16,4 +16,12 @@ from .attention import (  # noqa: F401
     v2_partition,
     v2_reduce,
 )
-from .metadata import cdiv, copy_page_indices, ext_device_core_count, log2_f32, num_kv_splits  # noqa: F401
+from .metadata import (  # noqa: F401
+    cdiv,
+    copy_page_indices,
+    decode_set_metadata,
+    ext_device_core_count,
+    log2_f32,
+    num_kv_splits,
+    wrap_int32,
+)

@@ -20,7 +20,8 @@ from typing import List, Sequence
 
 import numpy as np
 
-__all__ = ["copy_page_indices", "num_kv_splits", "ext_device_core_count", "log2_f32", "cdiv"]
+__all__ = ["copy_page_indices", "num_kv_splits", "ext_device_core_count", "log2_f32", "cdiv",
+           "decode_set_metadata", "wrap_int32"]
 
 
 def cdiv(a: int, b: int) -> int:
@@ -116,3 +117,55 @@ def num_kv_splits(seq_lens: Sequence[int], num_group: int, num_head: int, num_kv
         for i in range(num_group):
             out[s * num_group + i] = v
     return out
+
+
+def wrap_int32(v: int) -> int:
+    """Two's-complement int32 value of ``v`` (what a cast to int32 keeps)."""
+    v &= 0xFFFFFFFF
+    return v - (1 << 32) if v >= (1 << 31) else v
+
+
+def decode_set_metadata(seq_lens, req_to_token, req_pool_indices, max_seq_pages: int,
+                        seq_len_delta: int, page_size: int, full_to_swa_mapping=None):
+    """sglang ``normal_decode_set_metadata`` (python/sglang/kernels/ops/attention/
+    metadata.py) with its kernels ``_fused_metadata_kernel_general`` and
+    ``_fused_metadata_kernel_ps1_no_swa``, step by step:
+
+    1. ``cache_seqlens[i] = int32(seq_lens[i] + seq_len_delta)``;
+    2. ``cu_seqlens_k``: running int32 sum, ``cu[i]`` before adding entry i,
+       ``cu[B]`` the total;
+    3. ``page_index = req_to_token[req_pool_indices[i], c << SHIFT]`` for every
+       column ``c < max_seq_pages`` (``SHIFT = log2(page_size)``);
+    4. ``page_table[i, c] = page_index >> SHIFT``;
+    5. with a ``full_to_swa_mapping``: ``swa_page_table[i, c] =
+       full_to_swa_mapping[page_index] >> SHIFT``.
+
+    Returns ``(cache_seqlens, cu_seqlens_k, page_table, swa_page_table)`` as
+    Python lists (``swa_page_table`` is None without a mapping).
+    """
+    if page_size <= 0 or page_size & (page_size - 1):
+        raise ValueError("page_size must be a power of two")
+    shift = page_size.bit_length() - 1
+    B = len(seq_lens)
+    cache = []
+    cu = []
+    acc = 0
+    for i in range(B):
+        val = wrap_int32(int(seq_lens[i]) + seq_len_delta)
+        cache.append(val)
+        cu.append(acc)
+        acc = wrap_int32(acc + val)
+    cu.append(acc)
+    page_table, swa = [], ([] if full_to_swa_mapping is not None else None)
+    for i in range(B):
+        row = int(req_pool_indices[i])
+        pt_row, swa_row = [], []
+        for c in range(max_seq_pages):
+            page_index = int(req_to_token[row][c << shift])
+            pt_row.append(page_index >> shift)
+            if swa is not None:
+                swa_row.append(int(full_to_swa_mapping[page_index]) >> shift)
+        page_table.append(pt_row)
+        if swa is not None:
+            swa.append(swa_row)
+    return cache, cu, page_table, swa

@@ -484,3 +484,61 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_zero_query_gives_mean_of_values()
     monkeypatch.undo()
+
+
+# ------------------------------------------- metadata: fused decode metadata ---
+
+def _read_decode_metadata_example():
+    d = {"rt": {}}
+    for line in open(os.path.join(GOLDEN, "decode_set_metadata_example.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, val = line.split(":")
+        vals = [int(v) for v in val.split()]
+        if key.startswith("req_to_token"):
+            d["rt"][int(key.split()[1])] = vals
+        else:
+            d[key] = vals
+    return d
+
+
+def test_decode_set_metadata_golden():
+    d = _read_decode_metadata_example()
+    rt = [d["rt"][i] for i in range(len(d["rt"]))]
+    mapping = [100 + t for t in range(128)]
+    cache, cu, pt, swa = oracle.decode_set_metadata(
+        d["seq_lens"], rt, d["req_pool_indices"], d["max_seq_pages"][0], d["delta"][0],
+        d["page_size"][0], full_to_swa_mapping=mapping)
+    assert cache == d["expect cache_seqlens"]
+    assert cu == d["expect cu_seqlens_k"]
+    assert pt == [d["expect page_table 0"], d["expect page_table 1"]]
+    assert swa == [d["expect swa_page_table 0"], d["expect swa_page_table 1"]]
+
+
+@pytest.mark.parametrize("page_size", [1, 2, 16, 64])
+def test_decode_set_metadata_against_library_routines(page_size):
+    """cumsum for the indptr, floor division by the page size for the shift
+    (the docstring's "page_table = page_indices // page_size"), integer
+    indexing for both gathers."""
+    g = torch.Generator().manual_seed(page_size)
+    pool_rows, cols, B, msp = 9, 64 * page_size, 6, 40
+    rt = torch.randint(0, 1 << 20, (pool_rows, cols), generator=g, dtype=torch.int64)
+    pool = torch.randint(0, pool_rows, (B,), generator=g)
+    lens = torch.randint(0, 5000, (B,), generator=g)
+    mapping = torch.randint(0, 1 << 24, (1 << 20,), generator=g, dtype=torch.int64)
+    cache, cu, pt, swa = oracle.decode_set_metadata(lens.tolist(), rt.tolist(), pool.tolist(), msp,
+                                                    1, page_size, full_to_swa_mapping=mapping)
+    want_cache = (lens + 1).tolist()
+    assert cache == want_cache
+    assert cu == [0] + np.cumsum(want_cache).tolist()
+    page_index = rt[pool][:, ::page_size][:, :msp]
+    assert pt == torch.div(page_index, page_size, rounding_mode="floor").tolist()
+    assert swa == torch.div(mapping[page_index], page_size, rounding_mode="floor").tolist()
+
+
+def test_decode_set_metadata_int32_cast_wraps():
+    cache, cu, _, _ = oracle.decode_set_metadata([2 ** 31 - 1, 5], [[0]], [0, 0], 0, 1, 1)
+    want = np.array([2 ** 31 - 1, 5], dtype=np.int64) + 1
+    assert cache == want.astype(np.int32).tolist() == [-(2 ** 31), 6]
+    assert cu == [0, -(2 ** 31), -(2 ** 31) + 6]
