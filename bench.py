@@ -660,13 +660,135 @@ def run_ours(args):
     return 0
 
 
+def run_metadata(args):
+    """The fused decode metadata kernel alone (normal_decode_set_metadata), one
+    launch per step, L2 flushed between launches (its inputs are about L2-sized)."""
+    import ctypes
+
+    import paged_kv_decode_tables_gb300 as pkv
+    from paged_kv_decode_tables_gb300 import _build
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU for the library arm")
+    _build.build()
+    inp = workloads.make_decode_metadata_inputs(args.workload, seed=0, device="cuda")
+    B = inp["seq_lens"].shape[0]
+    msp, ps = inp["max_seq_pages"], inp["page_size"]
+    swa = inp["full_to_swa_mapping"] is not None
+    cache = torch.empty(B, dtype=torch.int32, device="cuda")
+    cu = torch.empty(B + 1, dtype=torch.int32, device="cuda")
+    pt = torch.empty(B, msp, dtype=torch.int32, device="cuda")
+    swa_t = torch.empty(B, msp, dtype=torch.int32, device="cuda") if swa else None
+    a = pkv.decode_metadata_args(cache, cu, pt, inp["req_to_token"], inp["req_pool_indices"],
+                                 inp["seq_lens"], seq_len_delta=inp["seq_len_delta"], page_size=ps,
+                                 max_seq_pages=msp, swa_page_table=swa_t,
+                                 full_to_swa_mapping=inp["full_to_swa_mapping"])
+    ref = ctypes.byref(a)
+    lib = pkv.lib()
+
+    def launch():
+        st = lib.normal_decode_set_metadata(ref, torch.cuda.current_stream().cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"normal_decode_set_metadata failed with status {st}")
+
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for _ in range(max(3, args.warmup)):
+        launch()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    for i in range(K):
+        flush_buf.fill_(float(i))
+        ev[i][0].record()
+        launch()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    ms = [x.elapsed_time(y) for x, y in ev]
+    avg_ms = sum(ms) / K
+    entries = B * msp
+    alg = (entries * 4 * 2 + (entries * (8 + 4) if swa else 0) + B * 8 * 2 + B * 4 + (B + 1) * 4)
+    peak, peak_kind = load_peak()
+    achieved = alg / (avg_ms * 1e-3) / 1e9
+
+    # end to end: lengths and request rows from pinned host memory, outputs back
+    h_lens = inp["seq_lens"].cpu().pin_memory()
+    h_pool = inp["req_pool_indices"].cpu().pin_memory()
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (cache, cu, pt)]
+    Ke = max(3, min(K, 100))
+    for it in range(Ke + 3):
+        if it == 3:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        inp["seq_lens"].copy_(h_lens, non_blocking=True)
+        inp["req_pool_indices"].copy_(h_pool, non_blocking=True)
+        launch()
+        for h, d in zip(h_out, (cache, cu, pt)):
+            h.copy_(d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_s = (time.perf_counter() - t0) / Ke
+    h2d = h_lens.numel() * 8 + h_pool.numel() * 8
+    d2h = sum(h.numel() * h.element_size() for h in h_out)
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        cores = cpu_threads()
+        rt = inp["req_to_token"].cpu()
+        mapping = inp["full_to_swa_mapping"].cpu() if swa else None
+        lens = inp["seq_lens"].cpu().tolist()
+        pool = inp["req_pool_indices"].cpu().tolist()
+        t0 = time.perf_counter()
+        rows = 0
+        while rows < B and time.perf_counter() - t0 < args.cpu_budget:
+            n = min(8, B - rows)
+            oracle.decode_set_metadata(lens[rows:rows + n], rt, pool[rows:rows + n], msp,
+                                       inp["seq_len_delta"], ps, full_to_swa_mapping=mapping)
+            rows += n
+        dt = time.perf_counter() - t0
+        per_row = alg / B
+        cpu = {"value": round(per_row * rows / dt / 1e9, 5), "unit": UNIT, "cores": 1,
+               "kind": "oracle",
+               "sample": f"{rows} of {B} request rows, pure Python, {dt:.1f} s"}
+        del cores
+
+    line = {
+        "metric": "fused decode metadata µs/launch and GB/s moved at 1 GPU",
+        "value": round(achieved, 2), "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(avg_ms, 5),
+        "us_per_step": round(avg_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic (seeded; see workloads.py)",
+        "config": {"workload": args.workload, "description": inp["description"],
+                   "batch": B, "page_size": ps, "max_seq_pages": msp, "swa": swa,
+                   "l2": "flushed between launches (512 MB write)"},
+        "roofline": {"kernel": "normal_decode_set_metadata", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "alg_bytes_per_launch": alg, "avg_launch_us": round(avg_ms * 1e3, 2)},
+        "e2e": {"value": round(alg / e2e_s / 1e9, 2), "unit": UNIT,
+                "us_per_step": round(e2e_s * 1e6, 2), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K, "clocks": clk, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.METADATA_WORKLOADS))
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="smaller batch of the same workload (profiling captures only)")
     ap.add_argument("--warps", type=int, default=0, choices=[0, 1, 2, 4],
@@ -682,6 +804,12 @@ def main(argv=None):
     ap.add_argument("--reference-budget", type=float, default=150.0,
                     help="total seconds for --impl reference")
     args = ap.parse_args(argv)
+    if args.workload in workloads.METADATA_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the "
+                              "decode workloads; this workload is a library addition"}))
+            return 0
+        return run_metadata(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

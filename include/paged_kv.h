@@ -263,6 +263,54 @@ pkv_status_t prepare_decode_metadata(int32_t *page_indices, int64_t page_indices
                                      int32_t *err_flag, pkv_stream_t stream);
 
 /*
+ * Fused decode metadata (sglang python/sglang/kernels/ops/attention/metadata.py,
+ * normal_decode_set_metadata with _fused_metadata_kernel_general and
+ * _fused_metadata_kernel_ps1_no_swa), one launch, no host sync.  With
+ * SHIFT = log2(page_size) and B = batch_size:
+ *   cache_seqlens[i]      = int32(seq_lens[i] + seq_len_delta)
+ *   cu_seqlens_k[i]       = cache_seqlens[0] + ... + cache_seqlens[i-1]  (int32, i <= B)
+ *   page_index            = req_to_token[req_pool_indices[i], c << SHIFT],  c < max_seq_pages
+ *   page_table[i, c]      = page_index >> SHIFT
+ *   swa_page_table[i, c]  = int32(full_to_swa_mapping[page_index] >> SHIFT)   (if given)
+ * Bit-exact.  Every column c < max_seq_pages of every row is written, as on
+ * the page.  All strides are in elements.  A pool row or column outside
+ * [0, req_to_token_rows) x [0, req_to_token_cols), or a page index outside
+ * [0, full_to_swa_len), writes 0 there and sets PKV_ERRF_INDPTR in err_flag.
+ * page_size must be a power of two; batch_size >= 1.
+ */
+typedef struct {
+  int32_t batch_size;
+  int32_t max_seq_pages;
+  int32_t seq_len_delta;
+  int32_t page_size;
+  const int64_t *seq_lens;
+  int64_t seq_lens_stride;
+  const int32_t *req_to_token;
+  int64_t req_to_token_stride[2];
+  int64_t req_to_token_rows;
+  int64_t req_to_token_cols;
+  const int64_t *req_pool_indices;
+  int64_t req_pool_indices_stride;
+  int32_t *cache_seqlens;
+  int64_t cache_seqlens_stride;
+  int32_t *cu_seqlens_k;
+  int64_t cu_seqlens_k_stride;
+  int32_t *page_table;
+  int64_t page_table_stride[2];
+  int32_t *swa_page_table;            /* optional (NULL: no sliding-window table) */
+  int64_t swa_page_table_stride[2];
+  const int64_t *full_to_swa_mapping; /* required with swa_page_table */
+  int64_t full_to_swa_stride;
+  int64_t full_to_swa_len;
+  int32_t *err_flag;                  /* optional */
+} pkv_decode_metadata_args_t;
+
+pkv_status_t normal_decode_set_metadata(const pkv_decode_metadata_args_t *args,
+                                        pkv_stream_t stream);
+/* sizeof(pkv_decode_metadata_args_t), for bindings that mirror the struct. */
+size_t pkv_decode_metadata_args_size(void);
+
+/*
  * Split-KV decode (partition pass + reduce) that allocates nothing.
  *
  * The pages have no counterpart of this entry point; it exists for callers

@@ -138,7 +138,7 @@ def decode_set_metadata(seq_lens, req_to_token, req_pool_indices, max_seq_pages:
        column ``c < max_seq_pages`` (``SHIFT = log2(page_size)``);
     4. ``page_table[i, c] = page_index >> SHIFT``;
     5. with a ``full_to_swa_mapping``: ``swa_page_table[i, c] =
-       full_to_swa_mapping[page_index] >> SHIFT``.
+       full_to_swa_mapping[page_index] >> SHIFT``, stored as int32.
 
     Returns ``(cache_seqlens, cu_seqlens_k, page_table, swa_page_table)`` as
     Python lists (``swa_page_table`` is None without a mapping).
@@ -164,7 +164,7 @@ def decode_set_metadata(seq_lens, req_to_token, req_pool_indices, max_seq_pages:
             page_index = int(req_to_token[row][c << shift])
             pt_row.append(page_index >> shift)
             if swa is not None:
-                swa_row.append(int(full_to_swa_mapping[page_index]) >> shift)
+                swa_row.append(wrap_int32(int(full_to_swa_mapping[page_index]) >> shift))
         page_table.append(pt_row)
         if swa is not None:
             swa.append(swa_row)

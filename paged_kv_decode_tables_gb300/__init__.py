@@ -30,6 +30,7 @@ __all__ = [
     "copy_page_indices",
     "compute_num_kv_splits",
     "prepare_decode_metadata",
+    "normal_decode_set_metadata",
     "paged_attention_v2_noalloc",
     "noalloc_scratch_bytes",
 ]
@@ -61,6 +62,26 @@ class DecodeArgs(ctypes.Structure):
         ("value_cache", _c_p), ("v_stride", _c_i64 * 4),
         ("block_tables", _c_p), ("bt_stride", _c_i64 * 2),
         ("kv_indptr", _c_p), ("seq_lens", _c_p), ("err_flag", _c_p),
+    ]
+
+
+class DecodeMetadataArgs(ctypes.Structure):
+    """Mirror of ``pkv_decode_metadata_args_t``."""
+
+    _fields_ = [
+        ("batch_size", _c_i32), ("max_seq_pages", _c_i32), ("seq_len_delta", _c_i32),
+        ("page_size", _c_i32),
+        ("seq_lens", _c_p), ("seq_lens_stride", _c_i64),
+        ("req_to_token", _c_p), ("req_to_token_stride", _c_i64 * 2),
+        ("req_to_token_rows", _c_i64), ("req_to_token_cols", _c_i64),
+        ("req_pool_indices", _c_p), ("req_pool_indices_stride", _c_i64),
+        ("cache_seqlens", _c_p), ("cache_seqlens_stride", _c_i64),
+        ("cu_seqlens_k", _c_p), ("cu_seqlens_k_stride", _c_i64),
+        ("page_table", _c_p), ("page_table_stride", _c_i64 * 2),
+        ("swa_page_table", _c_p), ("swa_page_table_stride", _c_i64 * 2),
+        ("full_to_swa_mapping", _c_p), ("full_to_swa_stride", _c_i64),
+        ("full_to_swa_len", _c_i64),
+        ("err_flag", _c_p),
     ]
 
 
@@ -109,6 +130,12 @@ def lib() -> ctypes.CDLL:
     L.prepare_decode_metadata.argtypes = [_c_p, _c_i64, _c_p, _c_i32, _c_i64, _c_i64, _c_p, _c_i32,
                                           _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p,
                                           _c_p]
+    L.pkv_decode_metadata_args_size.restype = ctypes.c_size_t
+    L.pkv_decode_metadata_args_size.argtypes = []
+    if L.pkv_decode_metadata_args_size() != ctypes.sizeof(DecodeMetadataArgs):
+        raise RuntimeError("pkv_decode_metadata_args_t layout mismatch")
+    L.normal_decode_set_metadata.restype = ctypes.c_int
+    L.normal_decode_set_metadata.argtypes = [ctypes.POINTER(DecodeMetadataArgs), _c_p]
     L.paged_attention_v2_noalloc.restype = ctypes.c_int
     L.paged_attention_v2_noalloc.argtypes = [_c_p, ctypes.POINTER(_c_i64), _c_i32, _c_i32, _c_p,
                                              ctypes.POINTER(DecodeArgs), _c_p]
@@ -345,6 +372,67 @@ def prepare_decode_metadata(page_indices: torch.Tensor, block_table: torch.Tenso
                                          int(num_kv_head), int(max_kv_splits),
                                          int(device_core_count), _ptr(err_flag), _stream(stream)),
            "prepare_decode_metadata")
+
+
+def decode_metadata_args(cache_seqlens, cu_seqlens_k, page_table, req_to_token, req_pool_indices,
+                         seq_lens, *, seq_len_delta: int, page_size: int,
+                         max_seq_pages: Optional[int] = None, swa_page_table=None,
+                         full_to_swa_mapping=None, err_flag=None) -> DecodeMetadataArgs:
+    """Fill the argument struct of ``normal_decode_set_metadata`` from tensors."""
+    checks = ((cache_seqlens, "cache_seqlens", torch.int32), (cu_seqlens_k, "cu_seqlens_k", torch.int32),
+              (page_table, "page_table", torch.int32), (req_to_token, "req_to_token", torch.int32),
+              (req_pool_indices, "req_pool_indices", torch.int64), (seq_lens, "seq_lens", torch.int64),
+              (swa_page_table, "swa_page_table", torch.int32),
+              (full_to_swa_mapping, "full_to_swa_mapping", torch.int64),
+              (err_flag, "err_flag", torch.int32))
+    for t, n, dt in checks:
+        _cuda(t, n)
+        if t is not None and t.dtype != dt:
+            raise ValueError(f"{n} must be {dt}")
+    B = seq_lens.shape[0]
+    if max_seq_pages is None:
+        max_seq_pages = page_table.shape[1]
+    if page_table.dim() != 2 or page_table.shape[0] < B or page_table.shape[1] < max_seq_pages:
+        raise ValueError("page_table must be at least [batch_size, max_seq_pages]")
+    if cu_seqlens_k.shape[0] < B + 1 or cache_seqlens.shape[0] < B or req_pool_indices.shape[0] < B:
+        raise ValueError("output / index tensors are too short for the batch")
+    a = DecodeMetadataArgs()
+    a.batch_size, a.max_seq_pages = B, int(max_seq_pages)
+    a.seq_len_delta, a.page_size = int(seq_len_delta), int(page_size)
+    a.seq_lens, a.seq_lens_stride = _ptr(seq_lens), seq_lens.stride(0)
+    a.req_to_token = _ptr(req_to_token)
+    a.req_to_token_stride[0], a.req_to_token_stride[1] = req_to_token.stride()
+    a.req_to_token_rows, a.req_to_token_cols = req_to_token.shape
+    a.req_pool_indices, a.req_pool_indices_stride = _ptr(req_pool_indices), req_pool_indices.stride(0)
+    a.cache_seqlens, a.cache_seqlens_stride = _ptr(cache_seqlens), cache_seqlens.stride(0)
+    a.cu_seqlens_k, a.cu_seqlens_k_stride = _ptr(cu_seqlens_k), cu_seqlens_k.stride(0)
+    a.page_table = _ptr(page_table)
+    a.page_table_stride[0], a.page_table_stride[1] = page_table.stride()
+    if swa_page_table is not None:
+        if full_to_swa_mapping is None:
+            raise ValueError("swa_page_table needs full_to_swa_mapping")
+        a.swa_page_table = _ptr(swa_page_table)
+        a.swa_page_table_stride[0], a.swa_page_table_stride[1] = swa_page_table.stride()
+        a.full_to_swa_mapping = _ptr(full_to_swa_mapping)
+        a.full_to_swa_stride = full_to_swa_mapping.stride(0)
+        a.full_to_swa_len = full_to_swa_mapping.shape[0]
+    a.err_flag = _ptr(err_flag)
+    return a
+
+
+def normal_decode_set_metadata(cache_seqlens, cu_seqlens_k, page_table, req_to_token,
+                               req_pool_indices, seq_lens, *, seq_len_delta: int, page_size: int,
+                               max_seq_pages: Optional[int] = None, swa_page_table=None,
+                               full_to_swa_mapping=None, err_flag=None, stream=None) -> None:
+    """Fused decode metadata: lengths + delta, their int32 indptr, the page
+    table gathered from ``req_to_token`` (and the sliding-window table)."""
+    a = decode_metadata_args(cache_seqlens, cu_seqlens_k, page_table, req_to_token,
+                             req_pool_indices, seq_lens, seq_len_delta=seq_len_delta,
+                             page_size=page_size, max_seq_pages=max_seq_pages,
+                             swa_page_table=swa_page_table, full_to_swa_mapping=full_to_swa_mapping,
+                             err_flag=err_flag)
+    _check(lib().normal_decode_set_metadata(ctypes.byref(a), _stream(stream)),
+           "normal_decode_set_metadata")
 
 
 def noalloc_scratch_bytes() -> int:

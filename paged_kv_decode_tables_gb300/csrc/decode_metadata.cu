@@ -1,0 +1,129 @@
+// Fused decode metadata (sglang python/sglang/kernels/ops/attention/metadata.py:
+// normal_decode_set_metadata with _fused_metadata_kernel_general and
+// _fused_metadata_kernel_ps1_no_swa), one launch, no host sync:
+//
+//   cache_seqlens[i] = int32(seq_lens[i] + seq_len_delta)
+//   cu_seqlens_k     = running int32 sum of cache_seqlens (cu[0] = 0, cu[B] = total)
+//   page_index       = req_to_token[req_pool_indices[i], c << SHIFT],  c < max_seq_pages
+//   page_table[i, c] = page_index >> SHIFT                     (SHIFT = log2(page_size))
+//   swa_page_table[i, c] = full_to_swa_mapping[page_index] >> SHIFT   (optional)
+//
+// Blocks [0, B * chunks) gather one 256-column chunk of one request row each
+// (a thread per column); the last block computes the lengths and the scan
+// with warp shuffles, 256 lengths at a time.  Row and column indices into the
+// token pool and the mapping are bounds-checked: an out-of-range index writes
+// 0 and sets PKV_ERRF_INDPTR.
+#include <cuda_runtime.h>
+
+#include "../../include/paged_kv.h"
+#include "pkv_launch.cuh"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kCols = 256;
+
+__global__ void __launch_bounds__(kCols) decode_metadata_kernel(const pkv_decode_metadata_args_t a,
+                                                                int shift, int chunks) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int tid = threadIdx.x;
+  const int64_t gather_blocks = int64_t(a.batch_size) * chunks;
+  if (int64_t(blockIdx.x) == gather_blocks) {
+    // lengths and their exclusive scan (int32 arithmetic, wrapping like a cast)
+    __shared__ unsigned warp_sum[kCols / 32];
+    __shared__ unsigned carry_s;
+    const int lane = tid & 31, warp = tid >> 5;
+    unsigned carry = 0;
+    for (int base = 0; base < a.batch_size; base += kCols) {
+      const int i = base + tid;
+      unsigned v = 0;
+      if (i < a.batch_size) {
+        v = unsigned(a.seq_lens[int64_t(i) * a.seq_lens_stride] + a.seq_len_delta);
+        a.cache_seqlens[int64_t(i) * a.cache_seqlens_stride] = int32_t(v);
+      }
+      unsigned incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) warp_sum[warp] = incl;
+      __syncthreads();
+      unsigned before = 0, total = 0;
+#pragma unroll
+      for (int w = 0; w < kCols / 32; ++w) {
+        const unsigned ws = warp_sum[w];
+        if (w < warp) before += ws;
+        total += ws;
+      }
+      if (i < a.batch_size)
+        a.cu_seqlens_k[int64_t(i) * a.cu_seqlens_k_stride] = int32_t(carry + before + incl - v);
+      carry += total;
+      __syncthreads();
+    }
+    if (tid == 0) {
+      carry_s = carry;
+      a.cu_seqlens_k[int64_t(a.batch_size) * a.cu_seqlens_k_stride] = int32_t(carry_s);
+    }
+    return;
+  }
+  const int i = int(blockIdx.x / unsigned(chunks));
+  const int c = int(blockIdx.x % unsigned(chunks)) * kCols + tid;
+  if (c >= a.max_seq_pages) return;
+  const int64_t row = a.req_pool_indices[int64_t(i) * a.req_pool_indices_stride];
+  const int64_t col = int64_t(c) << shift;
+  int32_t page_index = 0;
+  if (row >= 0 && row < a.req_to_token_rows && col < a.req_to_token_cols) {
+    page_index =
+        __ldcs(a.req_to_token + row * a.req_to_token_stride[0] + col * a.req_to_token_stride[1]);
+  } else {
+    flag_error(a.err_flag, 8u);
+  }
+  __stcs(a.page_table + int64_t(i) * a.page_table_stride[0] + int64_t(c) * a.page_table_stride[1],
+         page_index >> shift);
+  if (a.swa_page_table != nullptr) {
+    int64_t slot = 0;
+    if (page_index >= 0 && page_index < a.full_to_swa_len) {
+      slot = a.full_to_swa_mapping[int64_t(page_index) * a.full_to_swa_stride];
+    } else {
+      flag_error(a.err_flag, 8u);
+    }
+    __stcs(a.swa_page_table + int64_t(i) * a.swa_page_table_stride[0] +
+               int64_t(c) * a.swa_page_table_stride[1],
+           int32_t(slot >> shift));
+  }
+}
+
+}  // namespace
+
+}  // namespace pkv
+
+extern "C" size_t pkv_decode_metadata_args_size(void) {
+  return sizeof(pkv_decode_metadata_args_t);
+}
+
+extern "C" pkv_status_t normal_decode_set_metadata(const pkv_decode_metadata_args_t *a,
+                                                   pkv_stream_t stream) {
+  if (a == nullptr) return PKV_ERR_INVALID_ARG;
+  if (a->batch_size < 1 || a->max_seq_pages < 0) return PKV_ERR_INVALID_ARG;
+  if (a->page_size < 1 || (a->page_size & (a->page_size - 1)) != 0) return PKV_ERR_INVALID_ARG;
+  if (!a->seq_lens || !a->cache_seqlens || !a->cu_seqlens_k) return PKV_ERR_INVALID_ARG;
+  if (a->max_seq_pages > 0 && (!a->req_to_token || !a->req_pool_indices || !a->page_table))
+    return PKV_ERR_INVALID_ARG;
+  if (a->req_to_token_rows < 0 || a->req_to_token_cols < 0) return PKV_ERR_INVALID_ARG;
+  if (a->swa_page_table != nullptr && (a->full_to_swa_mapping == nullptr || a->full_to_swa_len < 0))
+    return PKV_ERR_INVALID_ARG;
+  int shift = 0;
+  while ((1 << shift) < a->page_size) ++shift;
+  const int chunks = (a->max_seq_pages + pkv::kCols - 1) / pkv::kCols;
+  const int64_t blocks = int64_t(a->batch_size) * chunks + 1;
+  if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+  return pkv::launch_programmatic(pkv::decode_metadata_kernel, dim3(unsigned(blocks)),
+                                  dim3(pkv::kCols), 0, reinterpret_cast<cudaStream_t>(stream), *a,
+                                  shift, chunks) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}

@@ -154,6 +154,19 @@ def test_reduce_and_metadata_reject_bad_arguments(lib):
                                        None) == 1
     assert lib.prepare_decode_metadata(p, 10, p, 4, 4, 1, p, 2, p, p, 1, 8, 32, 16, 148, None,
                                        None) == 1
+    import paged_kv_decode_tables_gb300 as pkv
+    m = pkv.DecodeMetadataArgs()
+    m.batch_size, m.max_seq_pages, m.page_size = 2, 4, 3  # page size not a power of two
+    m.seq_lens = m.cache_seqlens = m.cu_seqlens_k = m.req_to_token = p
+    m.req_pool_indices = m.page_table = p
+    assert lib.normal_decode_set_metadata(ctypes.byref(m), None) == 1
+    m.page_size = 16
+    m.swa_page_table = p  # without a mapping
+    assert lib.normal_decode_set_metadata(ctypes.byref(m), None) == 1
+    m.swa_page_table = None
+    m.batch_size = 0
+    assert lib.normal_decode_set_metadata(ctypes.byref(m), None) == 1
+    assert lib.normal_decode_set_metadata(None, None) == 1
     assert lib.pkv_set_attention_warps(3) == 1
     assert lib.pkv_set_attention_warps(0) == 0
 

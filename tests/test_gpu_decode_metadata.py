@@ -1,0 +1,99 @@
+"""GPU fused decode metadata (sglang normal_decode_set_metadata) against the
+oracle, bit-exact: page sizes 1..64, with and without the sliding-window
+table, strided outputs, wrap-around of the int32 cast, bad indices flagged."""
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_tables_gb300 as pkv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_kv_decode_tables_gb300 import _build
+    _build.build()
+
+
+def _case(B, page_size, msp, pool_rows=None, swa=False, seed=0, delta=1, strided=False):
+    g = torch.Generator().manual_seed(seed)
+    pool_rows = pool_rows or B + 3
+    cols = max(1, msp * page_size)
+    rt = torch.randint(0, 1 << 22, (pool_rows, cols), generator=g, dtype=torch.int32)
+    pool = torch.randperm(pool_rows, generator=g)[:B].to(torch.int64)
+    lens = torch.randint(0, cols + 1, (B,), generator=g, dtype=torch.int64)
+    mapping = torch.randint(0, 1 << 30, (1 << 22,), generator=g, dtype=torch.int64)
+    dev = "cuda"
+    cache = torch.full((B,), -9, dtype=torch.int32, device=dev)
+    cu_store = torch.full((2 * (B + 1),), -9, dtype=torch.int32, device=dev)
+    cu = cu_store[::2] if strided else cu_store[:B + 1]
+    pt_store = torch.full((B, msp + 5), -9, dtype=torch.int32, device=dev)
+    pt = pt_store[:, :msp] if msp else pt_store[:, :1]
+    swa_t = torch.full((B, max(msp, 1)), -9, dtype=torch.int32, device=dev) if swa else None
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.normal_decode_set_metadata(cache, cu, pt, rt.to(dev), pool.to(dev), lens.to(dev),
+                                   seq_len_delta=delta, page_size=page_size, max_seq_pages=msp,
+                                   swa_page_table=swa_t,
+                                   full_to_swa_mapping=mapping.to(dev) if swa else None,
+                                   err_flag=err)
+    want = oracle.decode_set_metadata(lens.tolist(), rt, pool.tolist(), msp, delta, page_size,
+                                      full_to_swa_mapping=mapping if swa else None)
+    return cache, cu, pt, swa_t, err, want, pt_store
+
+
+@pytest.mark.parametrize("page_size", [1, 2, 16, 64])
+@pytest.mark.parametrize("swa", [False, True])
+@pytest.mark.parametrize("B,msp", [(1, 1), (5, 300), (37, 513), (300, 64)])
+def test_decode_metadata_bit_exact(page_size, swa, B, msp):
+    cache, cu, pt, swa_t, err, want, pt_store = _case(B, page_size, msp, swa=swa,
+                                                      seed=B + page_size + msp)
+    torch.cuda.synchronize()
+    assert cache.cpu().tolist() == want[0]
+    assert cu.cpu().tolist() == want[1]
+    assert pt.cpu().tolist() == want[2]
+    if swa:
+        assert swa_t.cpu().tolist() == want[3]
+    assert bool((pt_store[:, msp:] == -9).all())  # columns past max_seq_pages untouched
+    assert int(err.item()) == 0
+
+
+def test_decode_metadata_strided_indptr_and_many_rows():
+    cache, cu, pt, _, err, want, _ = _case(3000, 16, 40, strided=True, seed=3, delta=0)
+    assert cu.cpu().tolist() == want[1]
+    assert cache.cpu().tolist() == want[0]
+    assert pt.cpu().tolist() == want[2]
+
+
+def test_decode_metadata_int32_wrap_and_zero_pages():
+    dev = "cuda"
+    lens = torch.tensor([2 ** 31 - 1, 5, 7], dtype=torch.int64, device=dev)
+    cache = torch.empty(3, dtype=torch.int32, device=dev)
+    cu = torch.empty(4, dtype=torch.int32, device=dev)
+    pt = torch.empty(3, 1, dtype=torch.int32, device=dev)
+    rt = torch.zeros(1, 1, dtype=torch.int32, device=dev)
+    pool = torch.zeros(3, dtype=torch.int64, device=dev)
+    pkv.normal_decode_set_metadata(cache, cu, pt, rt, pool, lens, seq_len_delta=1, page_size=1,
+                                   max_seq_pages=0)
+    want = oracle.decode_set_metadata(lens.tolist(), [[0]], [0, 0, 0], 0, 1, 1)
+    assert cache.cpu().tolist() == want[0]
+    assert cu.cpu().tolist() == want[1]
+
+
+def test_decode_metadata_flags_bad_pool_rows():
+    dev = "cuda"
+    lens = torch.tensor([10, 20], dtype=torch.int64, device=dev)
+    rt = torch.arange(16, dtype=torch.int32, device=dev).view(2, 8)
+    pool = torch.tensor([1, 5], dtype=torch.int64, device=dev)  # row 5 does not exist
+    cache = torch.empty(2, dtype=torch.int32, device=dev)
+    cu = torch.empty(3, dtype=torch.int32, device=dev)
+    pt = torch.full((2, 4), -1, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.normal_decode_set_metadata(cache, cu, pt, rt, pool, lens, seq_len_delta=0, page_size=2,
+                                   err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.PKV_ERRF_INDPTR
+    assert pt[0].cpu().tolist() == [4, 5, 6, 7]  # row 1: tokens 8,10,12,14 >> 1
+    assert pt[1].cpu().tolist() == [0, 0, 0, 0]

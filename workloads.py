@@ -320,3 +320,52 @@ def make_workload(name: str, seed: int = 0, device="cpu", **overrides) -> Dict:
     inp["cu_num_blocks"] = torch.tensor(cu, dtype=torch.int32, device=device)
     inp["spec"] = spec
     return inp
+
+
+# ------------------------------------------------ fused decode metadata inputs --
+
+METADATA_WORKLOADS = {
+    "decode_metadata_ps1": dict(
+        description=("fused decode metadata, page size 1, no sliding window: 512 requests "
+                     "(log-normal lengths as the ragged batch), token pool [1024, 32768] int32, "
+                     "max_seq_pages 32768, delta 1"),
+        batch=512, pool_rows=1024, pool_cols=32768, page_size=1, max_seq_pages=32768, swa=False),
+    "decode_metadata_ps16_swa": dict(
+        description=("fused decode metadata, page size 16 with the sliding-window table: 512 "
+                     "requests, token pool [1024, 32768] int32, max_seq_pages 2048, delta 1, "
+                     "full-to-SWA mapping of 2^25 int64 entries"),
+        batch=512, pool_rows=1024, pool_cols=32768, page_size=16, max_seq_pages=2048, swa=True),
+}
+
+
+def make_decode_metadata_inputs(name: str, seed: int = 0, device="cpu") -> Dict:
+    """Token pool, request rows, lengths (and SWA mapping) for one metadata launch.
+
+    ``req_to_token`` holds distinct token slot ids drawn as a seeded
+    permutation; requests use distinct pool rows; lengths follow the ragged
+    batch's log-normal recipe (clipped to the pool width).
+    """
+    cfg = METADATA_WORKLOADS[name]
+    g = _gen(seed, 7, "cpu")
+    B, rows, cols = cfg["batch"], cfg["pool_rows"], cfg["pool_cols"]
+    spec = WORKLOADS["ragged_v2_bf16"]
+    lens = _draw_seq_lens(WorkloadSpec(**{**spec.__dict__, "num_seqs": B,
+                                          "seq_len_hi": cols - 1}), seed)
+    gd = _gen(seed, 8, device)
+    req_to_token = torch.randint(0, rows * cols, (rows, cols), generator=gd, device=device,
+                                 dtype=torch.int32)
+    pool = torch.randperm(rows, generator=g)[:B].to(torch.int64).to(device)
+    out = {
+        "req_to_token": req_to_token,
+        "req_pool_indices": pool,
+        "seq_lens": torch.tensor(lens, dtype=torch.int64, device=device),
+        "page_size": cfg["page_size"],
+        "max_seq_pages": cfg["max_seq_pages"],
+        "seq_len_delta": 1,
+        "description": cfg["description"],
+        "full_to_swa_mapping": None,
+    }
+    if cfg["swa"]:
+        out["full_to_swa_mapping"] = torch.randint(0, 1 << 30, (rows * cols,), generator=gd,
+                                                   device=device, dtype=torch.int64)
+    return out
