@@ -8,9 +8,9 @@
 //   page_table[i, c] = page_index >> SHIFT                     (SHIFT = log2(page_size))
 //   swa_page_table[i, c] = full_to_swa_mapping[page_index] >> SHIFT   (optional)
 //
-// Blocks [0, B * chunks) gather one 256-column chunk of one request row each
-// (a thread per column); the last block computes the lengths and the scan
-// with warp shuffles, 256 lengths at a time.  Row and column indices into the
+// Blocks [0, B * chunks) gather one 2048-column chunk of one request row each
+// (eight columns per thread, their loads issued together); the last block
+// computes the lengths and the scan with warp shuffles, 256 at a time.  Row and column indices into the
 // token pool and the mapping are bounds-checked: an out-of-range index writes
 // 0 and sets PKV_ERRF_INDPTR.
 #include <cuda_runtime.h>
@@ -23,7 +23,9 @@ namespace pkv {
 
 namespace {
 
-constexpr int kCols = 256;
+constexpr int kCols = 256;                           // threads per block
+constexpr int kPerThread = 8;                        // columns per thread
+constexpr int kChunkCols = kCols * kPerThread;       // columns per block
 
 __global__ void __launch_bounds__(kCols) decode_metadata_kernel(const pkv_decode_metadata_args_t a,
                                                                 int shift, int chunks) {
@@ -71,29 +73,52 @@ __global__ void __launch_bounds__(kCols) decode_metadata_kernel(const pkv_decode
     return;
   }
   const int i = int(blockIdx.x / unsigned(chunks));
-  const int c = int(blockIdx.x % unsigned(chunks)) * kCols + tid;
-  if (c >= a.max_seq_pages) return;
+  const int c0 = int(blockIdx.x % unsigned(chunks)) * kChunkCols + tid;
   const int64_t row = a.req_pool_indices[int64_t(i) * a.req_pool_indices_stride];
-  const int64_t col = int64_t(c) << shift;
-  int32_t page_index = 0;
-  if (row >= 0 && row < a.req_to_token_rows && col < a.req_to_token_cols) {
-    page_index =
-        __ldcs(a.req_to_token + row * a.req_to_token_stride[0] + col * a.req_to_token_stride[1]);
-  } else {
-    flag_error(a.err_flag, 8u);
-  }
-  __stcs(a.page_table + int64_t(i) * a.page_table_stride[0] + int64_t(c) * a.page_table_stride[1],
-         page_index >> shift);
-  if (a.swa_page_table != nullptr) {
-    int64_t slot = 0;
-    if (page_index >= 0 && page_index < a.full_to_swa_len) {
-      slot = a.full_to_swa_mapping[int64_t(page_index) * a.full_to_swa_stride];
-    } else {
-      flag_error(a.err_flag, 8u);
+  const bool row_ok = row >= 0 && row < a.req_to_token_rows;
+  const int32_t *src = a.req_to_token + (row_ok ? row : 0) * a.req_to_token_stride[0];
+  // Column c = c0 + k * kCols: each warp touches 32 consecutive columns per k,
+  // and the kPerThread loads of a thread are issued before any is used.
+  int32_t page_index[kPerThread];
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    const int c = c0 + k * kCols;
+    const int64_t col = int64_t(c) << shift;
+    page_index[k] = 0;
+    if (c < a.max_seq_pages) {
+      if (row_ok && col < a.req_to_token_cols)
+        page_index[k] = __ldcs(src + col * a.req_to_token_stride[1]);
+      else
+        flag_error(a.err_flag, 8u);
     }
-    __stcs(a.swa_page_table + int64_t(i) * a.swa_page_table_stride[0] +
-               int64_t(c) * a.swa_page_table_stride[1],
-           int32_t(slot >> shift));
+  }
+  int64_t slot[kPerThread];
+  if (a.swa_page_table != nullptr) {
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      slot[k] = 0;
+      if (c0 + k * kCols < a.max_seq_pages) {
+        if (page_index[k] >= 0 && page_index[k] < a.full_to_swa_len)
+          slot[k] = a.full_to_swa_mapping[int64_t(page_index[k]) * a.full_to_swa_stride];
+        else
+          flag_error(a.err_flag, 8u);
+      }
+    }
+  }
+  int32_t *pt = a.page_table + int64_t(i) * a.page_table_stride[0];
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    const int c = c0 + k * kCols;
+    if (c < a.max_seq_pages) __stcs(pt + int64_t(c) * a.page_table_stride[1], page_index[k] >> shift);
+  }
+  if (a.swa_page_table != nullptr) {
+    int32_t *sp = a.swa_page_table + int64_t(i) * a.swa_page_table_stride[0];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int c = c0 + k * kCols;
+      if (c < a.max_seq_pages)
+        __stcs(sp + int64_t(c) * a.swa_page_table_stride[1], int32_t(slot[k] >> shift));
+    }
   }
 }
 
@@ -118,7 +143,7 @@ extern "C" pkv_status_t normal_decode_set_metadata(const pkv_decode_metadata_arg
     return PKV_ERR_INVALID_ARG;
   int shift = 0;
   while ((1 << shift) < a->page_size) ++shift;
-  const int chunks = (a->max_seq_pages + pkv::kCols - 1) / pkv::kCols;
+  const int chunks = (a->max_seq_pages + pkv::kChunkCols - 1) / pkv::kChunkCols;
   const int64_t blocks = int64_t(a->batch_size) * chunks + 1;
   if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
   return pkv::launch_programmatic(pkv::decode_metadata_kernel, dim3(unsigned(blocks)),
