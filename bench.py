@@ -80,11 +80,15 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha() -> str:
-    """Hash of the attention kernel's sources (the kernel the traffic figure describes)."""
+ATTENTION_SOURCES = ("attention_kernel.cuh", "pkv_ptx.cuh")
+METADATA_SOURCES = ("decode_metadata.cu", "pkv_ptx.cuh", "pkv_launch.cuh")
+
+
+def kernel_source_sha(files=ATTENTION_SOURCES) -> str:
+    """Hash of a kernel's source files (the kernel a traffic figure describes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_tables_gb300", "csrc")
-    for name in ("attention_kernel.cuh", "pkv_ptx.cuh"):
+    for name in files:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -92,14 +96,14 @@ def kernel_source_sha() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the attention kernel from a committed ncu
-    summary, only while the kernel sources are unchanged since the capture."""
+    """DRAM bytes per launch of the workload's dominant kernel from the committed
+    ncu record, only while that kernel's sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("source_sha") == kernel_source_sha():
+        if e and e.get("source_sha") == kernel_source_sha(tuple(e["source_files"])):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -770,7 +774,7 @@ def run_metadata(args):
         "roofline": {"kernel": "normal_decode_set_metadata", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload),
                      "alg_bytes_per_launch": alg, "avg_launch_us": round(avg_ms * 1e3, 2)},
         "e2e": {"value": round(alg / e2e_s / 1e9, 2), "unit": UNIT,
                 "us_per_step": round(e2e_s * 1e6, 2), "h2d_bytes_per_step": h2d,
