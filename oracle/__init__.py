@@ -23,5 +23,6 @@ from .metadata import (  # noqa: F401
     ext_device_core_count,
     log2_f32,
     num_kv_splits,
+    swa_spec_page_table,
     wrap_int32,
 )

@@ -21,7 +21,7 @@ from typing import List, Sequence
 import numpy as np
 
 __all__ = ["copy_page_indices", "num_kv_splits", "ext_device_core_count", "log2_f32", "cdiv",
-           "decode_set_metadata", "wrap_int32"]
+           "decode_set_metadata", "wrap_int32", "swa_spec_page_table"]
 
 
 def cdiv(a: int, b: int) -> int:
@@ -169,3 +169,34 @@ def decode_set_metadata(seq_lens, req_to_token, req_pool_indices, max_seq_pages:
         if swa is not None:
             swa.append(swa_row)
     return cache, cu, page_table, swa
+
+
+def swa_spec_page_table(dst, page_table_a, page_table_b, seq_len_a, seq_len_b,
+                        num_draft_tokens: int):
+    """sglang ``prepare_swa_spec_page_table_triton`` / ``_prepare_swa_spec_page_table_kernel``
+    (python/sglang/kernels/ops/attention/metadata.py): row ``m`` of the output
+    (one per draft token; ``bs_expand = bs * num_draft_tokens`` rows) is row
+    ``m // num_draft_tokens`` of table A, cut to that request's ``seq_len_a``,
+    followed by row ``m`` of table B, cut to ``seq_len_b[m]``.  With
+    ``la = seq_len_a[m // R]``, ``lb = seq_len_b[m]`` and widths ``LEN_A``,
+    ``LEN_B``, for every column ``n < min(la + lb, LEN_A + LEN_B)``:
+
+    * ``n < la``: ``A[m // R, n]`` if ``n < LEN_A`` else 0;
+    * otherwise, ``k = n - la``: ``B[m, k]`` if ``k < LEN_B`` else 0.
+
+    Columns at or beyond ``la + lb`` keep their old value.  ``dst`` is a list
+    of lists updated in place and returned.
+    """
+    R = num_draft_tokens
+    len_a = len(page_table_a[0]) if len(page_table_a) else 0
+    len_b = len(page_table_b[0]) if len(page_table_b) else 0
+    for m in range(len(seq_len_b)):
+        la = int(seq_len_a[m // R])
+        lb = int(seq_len_b[m])
+        for n in range(min(la + lb, len_a + len_b)):
+            if n < la:
+                dst[m][n] = int(page_table_a[m // R][n]) if n < len_a else 0
+            else:
+                k = n - la
+                dst[m][n] = int(page_table_b[m][k]) if k < len_b else 0
+    return dst

@@ -542,3 +542,60 @@ def test_decode_set_metadata_int32_cast_wraps():
     want = np.array([2 ** 31 - 1, 5], dtype=np.int64) + 1
     assert cache == want.astype(np.int32).tolist() == [-(2 ** 31), 6]
     assert cu == [0, -(2 ** 31), -(2 ** 31) + 6]
+
+
+# ------------------------------------------- metadata: SWA speculative table ---
+
+def _read_swa_example():
+    d = {"A": {}, "B": {}, "expect": {}}
+    for line in open(os.path.join(GOLDEN, "swa_spec_page_table_example.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, val = line.split(":")
+        vals = [int(v) for v in val.split()]
+        parts = key.split()
+        if parts[0] in ("A", "B", "expect"):
+            d[parts[0]][int(parts[1])] = vals
+        else:
+            d[key] = vals
+    return d
+
+
+def test_swa_spec_page_table_golden():
+    d = _read_swa_example()
+    A = [d["A"][i] for i in range(len(d["A"]))]
+    B = [d["B"][i] for i in range(len(d["B"]))]
+    dst = [[-1] * 7 for _ in range(4)]
+    oracle.swa_spec_page_table(dst, A, B, d["seq_len_a"], d["seq_len_b"], d["draft_tokens"][0])
+    assert dst == [d["expect"][i] for i in range(4)]
+
+
+def test_swa_spec_page_table_is_a_concatenation():
+    """Within the tables' widths the row is torch.cat of the two cut rows,
+    and nothing past the combined length is written."""
+    g = torch.Generator().manual_seed(5)
+    bs, R, LA, LB = 5, 3, 40, 9
+    A = torch.randint(0, 1000, (bs, LA), generator=g)
+    Bt = torch.randint(0, 1000, (bs * R, LB), generator=g)
+    la = torch.randint(0, LA + 1, (bs,), generator=g)
+    lb = torch.randint(0, LB + 1, (bs * R,), generator=g)
+    dst = [[-5] * (LA + LB) for _ in range(bs * R)]
+    oracle.swa_spec_page_table(dst, A.tolist(), Bt.tolist(), la.tolist(), lb.tolist(), R)
+    for m in range(bs * R):
+        a_len, b_len = int(la[m // R]), int(lb[m])
+        want = torch.cat([A[m // R, :a_len], Bt[m, :b_len]]).tolist()
+        assert dst[m][:a_len + b_len] == want
+        assert dst[m][a_len + b_len:] == [-5] * (LA + LB - a_len - b_len)
+
+
+def test_swa_spec_page_table_pads_past_table_widths_with_zero():
+    dst = [[-1] * 6]
+    oracle.swa_spec_page_table(dst, [[7, 8]], [[4, 5]], [3], [3], 1)
+    # la 3 > LEN_A 2: column 2 is 0; the B part starts at column 3 (k = 0);
+    # nothing is written at or past LEN_A + LEN_B = 4 columns
+    assert dst == [[7, 8, 0, 4, -1, -1]]
+    dst = [[-1] * 4]
+    oracle.swa_spec_page_table(dst, [[7, 8]], [[4, 5]], [1], [3], 1)
+    # la 1: column 0 from A; k = 0, 1 from B; k = 2 >= LEN_B: 0
+    assert dst == [[7, 4, 5, 0]]
