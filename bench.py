@@ -426,8 +426,10 @@ def run_reference(args):
     device = "cuda" if torch.cuda.is_available() else "cpu"
     inp = workloads.make_workload(args.workload, seed=0, device=device)
     cores = cpu_threads()
+    # the whole --steps K --warmup W run stays within the budget: each step
+    # processes sequences (at least one) for its share of it
     total_budget = args.reference_budget
-    per_step = max(0.5, total_budget / max(1, args.steps + args.warmup))
+    per_step = total_budget / max(1, args.steps + args.warmup)
     order = torch.randperm(len(inp["seq_lens_list"]), generator=torch.Generator().manual_seed(0))
     order = order.tolist()
     pos = 0
@@ -785,6 +787,61 @@ def run_metadata(args):
     return 0
 
 
+def run_swa_spec(args):
+    """The SWA speculative page-table kernel alone, L2 flushed between launches."""
+    import paged_kv_decode_tables_gb300 as pkv
+    from paged_kv_decode_tables_gb300 import _build
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU for the library arm")
+    _build.build()
+    inp = workloads.make_swa_spec_inputs(args.workload, seed=0, device="cuda")
+    A, Bt = inp["page_table_a"], inp["page_table_b"]
+    la, lb, R = inp["seq_len_a"], inp["seq_len_b"], inp["num_draft_tokens"]
+    rows, width = Bt.shape[0], A.shape[1] + Bt.shape[1]
+    dst = torch.zeros(rows, width, dtype=torch.int32, device="cuda")
+
+    def launch():
+        pkv.prepare_swa_spec_page_table(dst, A, Bt, la, lb, R)
+
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for _ in range(max(3, args.warmup)):
+        launch()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for i in range(K):
+        flush_buf.fill_(float(i))
+        ev[i][0].record()
+        launch()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    avg_ms = sum(x.elapsed_time(y) for x, y in ev) / K
+    la_rows = la.repeat_interleave(R).to(torch.int64)
+    written = int(torch.clamp(la_rows + lb.to(torch.int64), max=width).sum())
+    alg = written * 4 * 2 + la.numel() * 4 + lb.numel() * 4  # read + write each element
+    peak, peak_kind = load_peak()
+    achieved = alg / (avg_ms * 1e-3) / 1e9
+    line = {
+        "metric": "SWA speculative page table µs/launch and GB/s moved at 1 GPU",
+        "value": round(achieved, 2), "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(avg_ms, 5),
+        "us_per_step": round(avg_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic (seeded; see workloads.py)",
+        "config": {"workload": args.workload, "description": inp["description"],
+                   "l2": "flushed between launches (512 MB write)"},
+        "roofline": {"kernel": "prepare_swa_spec_page_table", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "alg_bytes_per_launch": alg, "avg_launch_us": round(avg_ms * 1e3, 2)},
+        "gpu_launches": K, "cpu_baseline": None, "e2e": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -792,7 +849,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.METADATA_WORKLOADS))
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.METADATA_WORKLOADS)
+                    + sorted(workloads.SWA_SPEC_WORKLOADS))
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="smaller batch of the same workload (profiling captures only)")
     ap.add_argument("--warps", type=int, default=0, choices=[0, 1, 2, 4],
@@ -805,9 +863,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the CPU baseline sample")
-    ap.add_argument("--reference-budget", type=float, default=150.0,
-                    help="total seconds for --impl reference")
+    ap.add_argument("--reference-budget", type=float, default=120.0,
+                    help="total seconds of oracle work for --impl reference (all steps)")
     args = ap.parse_args(argv)
+    if args.workload in workloads.SWA_SPEC_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the "
+                              "decode workloads; this workload is a library addition"}))
+            return 0
+        return run_swa_spec(args)
     if args.workload in workloads.METADATA_WORKLOADS:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the "

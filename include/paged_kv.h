@@ -311,6 +311,43 @@ pkv_status_t normal_decode_set_metadata(const pkv_decode_metadata_args_t *args,
 size_t pkv_decode_metadata_args_size(void);
 
 /*
+ * Sliding-window page table for speculative decoding (sglang
+ * python/sglang/kernels/ops/attention/metadata.py, prepare_swa_spec_page_table_triton
+ * and _prepare_swa_spec_page_table_kernel).  With R = num_draft_tokens,
+ * la = seq_len_a[m / R], lb = seq_len_b[m], for every output row
+ * m < bs * R and column n < min(la + lb, len_a + len_b):
+ *   dst[m, n] = n < la ? (n < len_a ? page_table_a[m / R, n] : 0)
+ *                      : (n - la < len_b ? page_table_b[m, n - la] : 0)
+ * Columns at or past min(la + lb, len_a + len_b) are left untouched (reading:
+ * the page's grid covers the combined width of the two tables).  Bit-exact.
+ *   page_table_a: [bs, len_a] int32; page_table_b: [bs * R, len_b] int32;
+ *   seq_len_a: [bs] int32; seq_len_b: [bs * R] int32;
+ *   dst: [bs * R, >= len_a + len_b] int32.  Strides in elements.
+ * A negative length counts as 0 and sets PKV_ERRF_SEQ_LEN.
+ */
+typedef struct {
+  int32_t bs;
+  int32_t num_draft_tokens;
+  int32_t len_a;
+  int32_t len_b;
+  const int32_t *page_table_a;
+  int64_t a_stride[2];
+  const int32_t *page_table_b;
+  int64_t b_stride[2];
+  const int32_t *seq_len_a;
+  int64_t seq_len_a_stride;
+  const int32_t *seq_len_b;
+  int64_t seq_len_b_stride;
+  int32_t *dst;
+  int64_t dst_stride[2];
+  int32_t *err_flag; /* optional */
+} pkv_swa_spec_args_t;
+
+pkv_status_t prepare_swa_spec_page_table(const pkv_swa_spec_args_t *args, pkv_stream_t stream);
+/* sizeof(pkv_swa_spec_args_t), for bindings that mirror the struct. */
+size_t pkv_swa_spec_args_size(void);
+
+/*
  * Split-KV decode (partition pass + reduce) that allocates nothing.
  *
  * The pages have no counterpart of this entry point; it exists for callers

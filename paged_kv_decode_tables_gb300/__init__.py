@@ -31,6 +31,7 @@ __all__ = [
     "compute_num_kv_splits",
     "prepare_decode_metadata",
     "normal_decode_set_metadata",
+    "prepare_swa_spec_page_table",
     "paged_attention_v2_noalloc",
     "noalloc_scratch_bytes",
 ]
@@ -85,6 +86,20 @@ class DecodeMetadataArgs(ctypes.Structure):
     ]
 
 
+class SwaSpecArgs(ctypes.Structure):
+    """Mirror of ``pkv_swa_spec_args_t``."""
+
+    _fields_ = [
+        ("bs", _c_i32), ("num_draft_tokens", _c_i32), ("len_a", _c_i32), ("len_b", _c_i32),
+        ("page_table_a", _c_p), ("a_stride", _c_i64 * 2),
+        ("page_table_b", _c_p), ("b_stride", _c_i64 * 2),
+        ("seq_len_a", _c_p), ("seq_len_a_stride", _c_i64),
+        ("seq_len_b", _c_p), ("seq_len_b_stride", _c_i64),
+        ("dst", _c_p), ("dst_stride", _c_i64 * 2),
+        ("err_flag", _c_p),
+    ]
+
+
 _LIB = None
 
 
@@ -134,6 +149,12 @@ def lib() -> ctypes.CDLL:
     L.pkv_decode_metadata_args_size.argtypes = []
     if L.pkv_decode_metadata_args_size() != ctypes.sizeof(DecodeMetadataArgs):
         raise RuntimeError("pkv_decode_metadata_args_t layout mismatch")
+    L.pkv_swa_spec_args_size.restype = ctypes.c_size_t
+    L.pkv_swa_spec_args_size.argtypes = []
+    if L.pkv_swa_spec_args_size() != ctypes.sizeof(SwaSpecArgs):
+        raise RuntimeError("pkv_swa_spec_args_t layout mismatch")
+    L.prepare_swa_spec_page_table.restype = ctypes.c_int
+    L.prepare_swa_spec_page_table.argtypes = [ctypes.POINTER(SwaSpecArgs), _c_p]
     L.normal_decode_set_metadata.restype = ctypes.c_int
     L.normal_decode_set_metadata.argtypes = [ctypes.POINTER(DecodeMetadataArgs), _c_p]
     L.paged_attention_v2_noalloc.restype = ctypes.c_int
@@ -433,6 +454,40 @@ def normal_decode_set_metadata(cache_seqlens, cu_seqlens_k, page_table, req_to_t
                              err_flag=err_flag)
     _check(lib().normal_decode_set_metadata(ctypes.byref(a), _stream(stream)),
            "normal_decode_set_metadata")
+
+
+def prepare_swa_spec_page_table(dst: torch.Tensor, page_table_a: torch.Tensor,
+                                page_table_b: torch.Tensor, seq_len_a: torch.Tensor,
+                                seq_len_b: torch.Tensor, num_draft_tokens: int, *,
+                                err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Row m of ``dst`` = row m // R of table A cut to its length, then row m of B."""
+    for t, n in ((dst, "dst"), (page_table_a, "page_table_a"), (page_table_b, "page_table_b"),
+                 (seq_len_a, "seq_len_a"), (seq_len_b, "seq_len_b"), (err_flag, "err_flag")):
+        _cuda(t, n)
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    bs = seq_len_a.shape[0]
+    R = int(num_draft_tokens)
+    if seq_len_b.shape[0] != bs * R:
+        raise ValueError("seq_len_b must have bs * num_draft_tokens entries")
+    LA, LB = page_table_a.shape[1], page_table_b.shape[1]
+    if page_table_a.shape[0] < bs or page_table_b.shape[0] < bs * R:
+        raise ValueError("page tables have too few rows")
+    if dst.shape[0] < bs * R or dst.shape[1] < LA + LB:
+        raise ValueError("dst must be at least [bs * num_draft_tokens, len_a + len_b]")
+    a = SwaSpecArgs()
+    a.bs, a.num_draft_tokens, a.len_a, a.len_b = bs, R, LA, LB
+    a.page_table_a = _ptr(page_table_a)
+    a.a_stride[0], a.a_stride[1] = page_table_a.stride()
+    a.page_table_b = _ptr(page_table_b)
+    a.b_stride[0], a.b_stride[1] = page_table_b.stride()
+    a.seq_len_a, a.seq_len_a_stride = _ptr(seq_len_a), seq_len_a.stride(0)
+    a.seq_len_b, a.seq_len_b_stride = _ptr(seq_len_b), seq_len_b.stride(0)
+    a.dst = _ptr(dst)
+    a.dst_stride[0], a.dst_stride[1] = dst.stride()
+    a.err_flag = _ptr(err_flag)
+    _check(lib().prepare_swa_spec_page_table(ctypes.byref(a), _stream(stream)),
+           "prepare_swa_spec_page_table")
 
 
 def noalloc_scratch_bytes() -> int:

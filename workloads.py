@@ -369,3 +369,26 @@ def make_decode_metadata_inputs(name: str, seed: int = 0, device="cpu") -> Dict:
         out["full_to_swa_mapping"] = torch.randint(0, 1 << 30, (rows * cols,), generator=gd,
                                                    device=device, dtype=torch.int64)
     return out
+
+
+SWA_SPEC_WORKLOADS = {
+    "swa_spec_page_table": dict(
+        description=("sliding-window speculative page table: 128 requests x 4 draft tokens, "
+                     "table A [128, 4096] int32 (window pages), table B [512, 64] int32 "
+                     "(draft pages), lengths uniform in [0, width]"),
+        bs=128, draft_tokens=4, len_a=4096, len_b=64),
+}
+
+
+def make_swa_spec_inputs(name: str, seed: int = 0, device="cpu") -> Dict:
+    """Tables A and B and their per-row lengths for one SWA speculative table launch."""
+    cfg = SWA_SPEC_WORKLOADS[name]
+    g = _gen(seed, 9, "cpu")
+    bs, R, LA, LB = cfg["bs"], cfg["draft_tokens"], cfg["len_a"], cfg["len_b"]
+    A = torch.randint(0, 1 << 30, (bs, LA), generator=g, dtype=torch.int32)
+    B = torch.randint(0, 1 << 30, (bs * R, LB), generator=g, dtype=torch.int32)
+    la = torch.randint(0, LA + 1, (bs,), generator=g, dtype=torch.int32)
+    lb = torch.randint(0, LB + 1, (bs * R,), generator=g, dtype=torch.int32)
+    return {"page_table_a": A.to(device), "page_table_b": B.to(device),
+            "seq_len_a": la.to(device), "seq_len_b": lb.to(device), "num_draft_tokens": R,
+            "description": cfg["description"]}
