@@ -16,13 +16,14 @@
 
 #include "../../include/paged_kv.h"
 
+static constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB per GPU
+
+// The scratch itself: one file-scope array per GPU that loads the library.
+static __device__ __align__(256) unsigned char g_split_scratch[kScratchBytes];
+
 namespace {
 
-constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB per GPU
 constexpr size_t kAlign = 256;
-
-__device__ __align__(256) unsigned char g_split_scratch[kScratchBytes];
-
 constexpr int kMaxDevices = 64;
 std::atomic<void *> g_scratch_addr[kMaxDevices];
 
