@@ -1,0 +1,135 @@
+"""Randomised and extreme-size GPU parity against the float64 oracle.
+
+* A seeded sweep over dtype, head size, block size, GQA group, single pass /
+  fixed partitions / split counts, strided query and output views, column-step
+  block tables and warps per CTA.
+* A cache of about 10 GB per tensor whose last blocks hold a sequence, so that
+  element offsets pass 2^32 (64-bit address arithmetic in the bulk copies).
+* One 128k-token sequence decoded in a single pass.
+"""
+import random
+
+import pytest
+import torch
+
+import bench
+import oracle
+import paged_kv_decode_tables_gb300 as pkv
+import workloads
+from gpu_support import assert_attention_close, on_device
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_kv_decode_tables_gb300 import _build
+    _build.build()
+    yield
+    pkv.set_attention_warps(0)
+
+
+def _strided_like(t, rng):
+    """A view with the same shape as ``t`` but a padded innermost stride."""
+    pad = rng.choice([0, 8, 24])
+    B, H, D = t.shape
+    store = torch.zeros(B, H, D + pad, dtype=t.dtype, device=t.device)
+    v = store[:, :, :D]
+    v.copy_(t)
+    return v
+
+
+CASES = 48
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_random_configuration(case):
+    rng = random.Random(1000 + case)
+    dtype = rng.choice(["f16", "bf16", "f32"])
+    D = rng.choice([64, 128] if dtype == "f32" else [64, 128, 256])
+    bs = rng.choice([8, 16, 32])
+    Hk = rng.choice([1, 2, 4])
+    g = rng.choice([1, 2, 3, 4, 5, 8])
+    B = rng.randint(1, 6)
+    lens = [rng.choice([0, 1, bs, 16, 2 * bs + 1, rng.randint(1, 700)]) for _ in range(B)]
+    if max(lens) == 0:
+        lens[0] = 5
+    mode = rng.choice(["v1", "fixed", "splits"])
+    warps = rng.choice([0, 1, 2, 4])
+    inp = workloads.make_inputs(num_heads=Hk * g, num_kv_heads=Hk, head_size=D, block_size=bs,
+                                dtype=dtype, seq_lens=lens, seed=case,
+                                bt_col_step=rng.choice([1, 2]), peaky_fraction=0.01)
+    gd = on_device(inp)
+    q = _strided_like(gd["query"], rng)
+    out_ref = oracle.decode_v1(inp["query"], inp["key_cache"], inp["value_cache"],
+                               inp["block_tables"], lens, inp["scale"])
+    out = _strided_like(torch.zeros_like(gd["query"]), rng)
+    pkv.set_attention_warps(warps)
+    try:
+        if mode == "v1":
+            pkv.paged_attention_decode(out, q, gd["key_cache"], gd["value_cache"],
+                                       gd["block_tables"], gd["seq_lens"], inp["scale"])
+        else:
+            Bq, H, _ = q.shape
+            cap = inp["max_blocks_per_seq"] * bs
+            if mode == "fixed":
+                P = bs * rng.choice([1, 2, 4, 32])
+                maxP = -(-cap // P)
+                splits = None
+            else:
+                P = 512
+                maxP = rng.randint(1, 12)
+                splits = torch.tensor([rng.randint(1, maxP) for _ in range(B)], dtype=torch.int32,
+                                      device="cuda")
+            tmp = torch.empty(Bq, H, maxP, D, dtype=torch.float32, device="cuda")
+            es = torch.empty(Bq, H, maxP, dtype=torch.float32, device="cuda")
+            ml = torch.empty(Bq, H, maxP, dtype=torch.float32, device="cuda")
+            pkv.paged_attention_v2_partition(tmp, es, ml, q, gd["key_cache"], gd["value_cache"],
+                                             gd["block_tables"], gd["seq_lens"], inp["scale"],
+                                             partition_size=P, num_kv_splits=splits)
+            pkv.paged_attention_v2_reduce(out, tmp, es, ml, gd["seq_lens"], partition_size=P,
+                                          num_kv_splits=splits, block_size=bs)
+    finally:
+        pkv.set_attention_warps(0)
+    torch.cuda.synchronize()
+    assert_attention_close(out, out_ref, DT[dtype],
+                           f"case {case}: {dtype} D{D} bs{bs} {Hk}x{g} {mode} w{warps} {lens}")
+
+
+def test_offsets_beyond_four_gigabytes():
+    """Sequence 0 lives in the last blocks of a cache of 300,000 blocks
+    (each tensor 9.8 GB; its element offsets exceed 2^32)."""
+    NB, Hk, D, bs = 300_000, 8, 128, 16
+    lens = [64, 100, 37]
+    last = list(range(NB - 4, NB))
+    inp = workloads.make_inputs(num_heads=32, num_kv_heads=Hk, head_size=D, block_size=bs,
+                                dtype="bf16", seq_lens=lens, num_blocks=NB, first_row=last[::-1],
+                                seed=7, device="cuda")
+    assert int(inp["block_tables"][0].max()) * Hk * D * bs > 2 ** 32
+    out = torch.empty_like(inp["query"])
+    pkv.paged_attention_decode(out, inp["query"], inp["key_cache"], inp["value_cache"],
+                               inp["block_tables"], inp["seq_lens"], inp["scale"])
+    torch.cuda.synchronize()
+    q, kc, vc, bt, ls = bench.oracle_sample_inputs(inp, [0, 1, 2])
+    ref = oracle.decode_v1(q, kc, vc, bt, ls, inp["scale"])
+    assert_attention_close(out, ref, torch.bfloat16, "offsets beyond 2^32")
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_single_pass_128k_tokens():
+    lens = [131072]
+    inp = workloads.make_inputs(num_heads=8, num_kv_heads=1, head_size=128, block_size=16,
+                                dtype="bf16", seq_lens=lens, seed=8, device="cuda",
+                                peaky_fraction=0.01)
+    out = torch.empty_like(inp["query"])
+    pkv.paged_attention_decode(out, inp["query"], inp["key_cache"], inp["value_cache"],
+                               inp["block_tables"], inp["seq_lens"], inp["scale"])
+    torch.cuda.synchronize()
+    q, kc, vc, bt, ls = bench.oracle_sample_inputs(inp, [0])
+    ref = oracle.decode_v1(q, kc, vc, bt, ls, inp["scale"])
+    assert_attention_close(out, ref, torch.bfloat16, "128k single pass")
