@@ -129,6 +129,23 @@ size_t pkv_decode_args_size(void);
 pkv_status_t pkv_set_attention_warps(int32_t warps);
 
 /*
+ * Limit, in nanoseconds, of every wait of the attention kernels for a stage's
+ * copies into shared memory (default 2 s; 0 restores it; at most 60 s).  A
+ * wait that runs out sets PKV_ERRF_TIMEOUT, waits (again bounded) for the
+ * warp's other copies and finishes the CTA with unspecified results for it;
+ * no kernel ever waits without a limit.  Process-wide.
+ */
+pkv_status_t pkv_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook for the timeout path above: every stage of the attention kernels
+ * then expects `bytes` (a multiple of 16, at most 65536) more than its copies
+ * deliver, so each of its waits runs into the limit.  0 (default) turns it
+ * off.  Only for exercising failure detection; process-wide.
+ */
+pkv_status_t pkv_test_set_unarrived_bytes(uint32_t bytes);
+
+/*
  * Single-pass paged decode.
  *
  * For every sequence s and query head h:

@@ -125,6 +125,10 @@ def lib() -> ctypes.CDLL:
     L.pkv_decode_args_size.argtypes = []
     L.pkv_set_attention_warps.restype = ctypes.c_int
     L.pkv_set_attention_warps.argtypes = [_c_i32]
+    L.pkv_set_wait_limit_ns.restype = ctypes.c_int
+    L.pkv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.pkv_test_set_unarrived_bytes.restype = ctypes.c_int
+    L.pkv_test_set_unarrived_bytes.argtypes = [ctypes.c_uint32]
     L.paged_attention_decode.restype = ctypes.c_int
     L.paged_attention_decode.argtypes = [_c_p, ctypes.POINTER(_c_i64), ctypes.POINTER(DecodeArgs),
                                          _c_p]
@@ -198,6 +202,16 @@ def _stream(stream) -> int:
 def set_attention_warps(warps: int) -> None:
     """Force warps per CTA (1 or 4) for the attention kernels; 0 restores the default."""
     _check(lib().pkv_set_attention_warps(int(warps)), "pkv_set_attention_warps")
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of every copy wait in the attention kernels (0: the 2 s default)."""
+    _check(lib().pkv_set_wait_limit_ns(int(ns)), "pkv_set_wait_limit_ns")
+
+
+def _test_set_unarrived_bytes(nbytes: int) -> None:
+    """Test hook: stages expect ``nbytes`` that never arrive, so waits time out."""
+    _check(lib().pkv_test_set_unarrived_bytes(int(nbytes)), "pkv_test_set_unarrived_bytes")
 
 
 def _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,

@@ -18,6 +18,8 @@ using pkv::AttnParams;
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_forced_warps{0};
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+std::atomic<unsigned> g_extra_expect_tx{0};
 
 int sm_count() {
   int dev = 0;
@@ -108,6 +110,8 @@ AttnParams make_params(const pkv_decode_args_t *a) {
   p.num_blocks = a->num_blocks;
   p.max_blocks_per_seq = a->max_blocks_per_seq;
   p.scale_log2 = a->scale * 1.44269504088896340736f;
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.extra_expect_tx = g_extra_expect_tx.load(std::memory_order_relaxed);
   return p;
 }
 
@@ -145,6 +149,19 @@ size_t pkv_decode_args_size(void) { return sizeof(pkv_decode_args_t); }
 pkv_status_t pkv_set_attention_warps(int32_t warps) {
   if (warps != 0 && warps != 1 && warps != 2 && warps != 4) return PKV_ERR_INVALID_ARG;
   g_forced_warps.store(warps, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+pkv_status_t pkv_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) ns = 2000000000ull;
+  if (ns > 60000000000ull) return PKV_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+pkv_status_t pkv_test_set_unarrived_bytes(uint32_t bytes) {
+  if (bytes % 16 != 0 || bytes > 65536) return PKV_ERR_INVALID_ARG;
+  g_extra_expect_tx.store(bytes, std::memory_order_relaxed);
   return PKV_OK;
 }
 

@@ -61,6 +61,8 @@ struct AttnParams {
   float *tmp, *es, *ml;  // v2 outputs
   int32_t max_parts, partition_size;
   const int32_t *splits;
+  uint64_t wait_limit_ns;    // limit of every wait for a stage's copies
+  uint32_t extra_expect_tx;  // test hook: bytes a stage expects that never arrive (0)
 };
 
 constexpr int kMaxGroup = 8;
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
       for (int j = 0; j < PPC; ++j) np += id[j] >= 0 ? 1u : 0u;
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&bars[st], np * 2u * Cfg::kPageBytes);
+      mbar_arrive_expect_tx(&bars[st], np * 2u * Cfg::kPageBytes + p.extra_expect_tx);
 #pragma unroll
       for (int j = 0; j < PPC; ++j) {
         if (id[j] >= 0) {
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     const int jm = lane >> 3, rr = lane & 7;
     for (int i = 0; i < my_n; ++i) {
       const int st = i % NST;
-      const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u);
+      const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u, p.wait_limit_ns);
       if (!__all_sync(FULL, got)) {
         ok = false;
         break;
@@ -417,7 +419,8 @@ __global__ void __launch_bounds__(WARPS * 32)
     if (!ok) {
       if (lane == 0) flag_error(p.err, 16u);
       for (int i = waited; i < issued; ++i)
-        mbar_wait_bounded(&bars[i % NST], uint32_t(i / NST) & 1u, 100000000ull);
+        mbar_wait_bounded(&bars[i % NST], uint32_t(i / NST) & 1u,
+                          min(p.wait_limit_ns, uint64_t(100000000ull)));
       __syncwarp();
     }
     // Stage memory of this warp is free now: store O (as [head][dim]), m, l.
@@ -457,7 +460,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     for (int i = 0; i < my_n; ++i) {
       const int st = i % NST;
-      const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u);
+      const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u, p.wait_limit_ns);
       if (!__all_sync(FULL, got)) {
         ok = false;
         break;
@@ -501,7 +504,8 @@ __global__ void __launch_bounds__(WARPS * 32)
     if (!ok) {
       if (lane == 0) flag_error(p.err, 16u);
       for (int i = waited; i < issued; ++i)
-        mbar_wait_bounded(&bars[i % NST], uint32_t(i / NST) & 1u, 100000000ull);
+        mbar_wait_bounded(&bars[i % NST], uint32_t(i / NST) & 1u,
+                          min(p.wait_limit_ns, uint64_t(100000000ull)));
       __syncwarp();
     }
 #pragma unroll

@@ -167,6 +167,10 @@ def test_reduce_and_metadata_reject_bad_arguments(lib):
     m.batch_size = 0
     assert lib.normal_decode_set_metadata(ctypes.byref(m), None) == 1
     assert lib.normal_decode_set_metadata(None, None) == 1
+    assert lib.pkv_set_wait_limit_ns(61 * 10 ** 9) == 1
+    assert lib.pkv_set_wait_limit_ns(0) == 0
+    assert lib.pkv_test_set_unarrived_bytes(17) == 1
+    assert lib.pkv_test_set_unarrived_bytes(0) == 0
     assert lib.pkv_set_attention_warps(3) == 1
     assert lib.pkv_set_attention_warps(0) == 0
 

@@ -287,3 +287,29 @@ def test_bad_device_data_sets_flags_without_faulting():
     assert int(err.item()) & pkv.PKV_ERRF_SPLITS
     # the context is still usable
     assert_attention_close(run_v1(g), _oracle_v1(inp), torch.bfloat16, "after errors")
+
+
+def test_copy_wait_timeout_is_reported_and_the_context_survives():
+    """Failure detection without a fault: with the test hook every stage
+    expects 16 bytes that never arrive, so each bounded wait runs out (20 ms
+    here); the kernel reports PKV_ERRF_TIMEOUT and finishes, and the next
+    launches in the same context are correct."""
+    cases = [("bf16", 128, 16, 4, 1, [64]), ("f32", 64, 8, 4, 4, [16, 13])]
+    for dtype, D, bs, H, Hk, lens in cases:
+        inp = _inputs(dtype, D, bs, H, Hk, lens, seed=50)
+        g = on_device(inp)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pkv.set_wait_limit_ns(20_000_000)
+        pkv._test_set_unarrived_bytes(16)
+        try:
+            run_v1(g, err=err)
+            torch.cuda.synchronize()
+        finally:
+            pkv._test_set_unarrived_bytes(0)
+            pkv.set_wait_limit_ns(0)
+        assert int(err.item()) & pkv.PKV_ERRF_TIMEOUT, dtype
+        err.zero_()
+        out = run_v1(g, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_attention_close(out, _oracle_v1(inp), DT[dtype], f"after timeout {dtype}")
