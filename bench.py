@@ -314,7 +314,8 @@ class DecodeStep:
         hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         return hin, hout
 
-    def e2e_step(self, hin, hout):
+    def e2e_enqueue(self, hin, hout):
+        """H2D of the step's inputs, the step, D2H of its output (enqueued only)."""
         inp = self.inp
         inp["query"].copy_(hin["query"], non_blocking=True)
         inp["seq_lens"].copy_(hin["seq_lens"], non_blocking=True)
@@ -323,6 +324,15 @@ class DecodeStep:
             self.cu.copy_(hin["cu"], non_blocking=True)
         self.run()
         hout.copy_(self.out, non_blocking=True)
+
+    def e2e_step(self, hin, hout, graph=None):
+        """One end-to-end step; the host waits for the output.  With ``graph``
+        (a capture of ``e2e_enqueue``) the same copies and launches replay as
+        one graph launch."""
+        if graph is not None:
+            graph.replay()
+        else:
+            self.e2e_enqueue(hin, hout)
         torch.cuda.current_stream().synchronize()
 
     def e2e_bytes(self, hin, hout):
@@ -354,10 +364,13 @@ def oracle_sample_inputs(step_or_inp, seq_ids):
 
 def oracle_step(inp, spec, seq_ids, all_splits):
     """The oracle's pass over the sampled sequences (the same steps as the
-    GPU step: metadata, then split-KV partition + reduce or single pass)."""
+    GPU step: metadata, then split-KV partition + reduce or single pass).
+    Returns (K/V bytes covered, seconds spent in the oracle itself); copying
+    the sampled pages out of device memory is not counted."""
     import oracle
 
     q, kc, vc, bt, lens = oracle_sample_inputs(inp, seq_ids)
+    t0 = time.perf_counter()
     if spec.mode == "v1":
         oracle.decode_v1(q, kc, vc, bt, lens, inp["scale"])
     elif spec.mode == "v2_fixed":
@@ -370,8 +383,9 @@ def oracle_step(inp, spec, seq_ids, all_splits):
         tmp, es, ml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], spec.max_kv_splits,
                                           num_kv_splits=splits)
         oracle.v2_reduce(tmp, es, ml, lens, spec.block_size, num_kv_splits=splits)
+    dt = time.perf_counter() - t0
     e = inp["query"].element_size()
-    return sum(lens) * spec.num_kv_heads * 2 * spec.head_size * e
+    return sum(lens) * spec.num_kv_heads * 2 * spec.head_size * e, dt
 
 
 def cpu_threads():
@@ -398,22 +412,27 @@ def oracle_metadata(inp, spec):
 
 def cpu_baseline(inp, spec, budget_s=10.0):
     """The oracle on a bounded sample: sequences in a seeded order until the
-    time budget is spent; returns KV-read GB/s over the sample."""
+    oracle has spent the time budget (after one untimed warm-up sequence);
+    returns KV-read GB/s over the sample."""
     cores = cpu_threads()
     order = torch.randperm(len(inp["seq_lens_list"]), generator=torch.Generator().manual_seed(0))
+    order = order.tolist()
     t0 = time.perf_counter()
     splits = oracle_metadata(inp, spec)
+    spent = time.perf_counter() - t0
+    oracle_step(inp, spec, [order[-1]], splits)  # warm-up, not counted
     done, nbytes = [], 0
-    for s in order.tolist():
-        nbytes += oracle_step(inp, spec, [s], splits)
+    for s in order:
+        nb, dt = oracle_step(inp, spec, [s], splits)
+        nbytes += nb
+        spent += dt
         done.append(s)
-        if time.perf_counter() - t0 >= budget_s:
+        if spent >= budget_s:
             break
-    dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": nbytes / spent / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": (f"{len(done)} of {len(inp['seq_lens_list'])} sequences "
                        f"({nbytes / 1e9:.3f} GB of K/V) of {spec.name} plus the whole batch's "
-                       f"metadata, float64, {dt:.1f} s")}
+                       f"metadata, float64, {spent:.1f} s of oracle time")}
 
 
 # ------------------------------------------------------------------ arms --
@@ -437,15 +456,16 @@ def run_reference(args):
 
     def one_step():
         nonlocal pos
-        t0 = time.perf_counter()
-        nb, n = 0, 0
+        nb, n, spent = 0, 0, 0.0
         while True:
-            nb += oracle_step(inp, spec, [order[pos % len(order)]], splits)
+            b, dt = oracle_step(inp, spec, [order[pos % len(order)]], splits)
+            nb += b
+            spent += dt
             pos += 1
             n += 1
-            if time.perf_counter() - t0 >= per_step:
+            if spent >= per_step:
                 break
-        return nb, time.perf_counter() - t0, n
+        return nb, spent, n
 
     for _ in range(args.warmup):
         one_step()
@@ -579,13 +599,23 @@ def run_ours(args):
     # D2H of the output, host waits for it)
     hin, hout = step.host_inputs()
     Ke = max(3, min(K, 200))
+    e2e_graph = None
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step.e2e_enqueue(hin, hout)
+        torch.cuda.current_stream().wait_stream(side)
+        e2e_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(e2e_graph):
+            step.e2e_enqueue(hin, hout)
     for _ in range(3):
-        step.e2e_step(hin, hout)
+        step.e2e_step(hin, hout, e2e_graph)
     if dist is not None:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(Ke):
-        step.e2e_step(hin, hout)
+        step.e2e_step(hin, hout, e2e_graph)
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, dist, "cuda")
     h2d, d2h = step.e2e_bytes(hin, hout)
@@ -655,7 +685,10 @@ def run_ours(args):
         "e2e": {"value": round(aggregate_gbs(step.kv_bytes, world, e2e_s / Ke), 2), "unit": UNIT,
                 "us_per_step": round(e2e_s / Ke * 1e6, 2), "steps": Ke,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "K/V cache resident on the device; per-step inputs from pinned host memory"},
+                "note": ("K/V cache resident on the device; per step: H2D of the inputs from "
+                         "pinned host memory, the step, D2H of the output, host waits"
+                         + ("; replayed as one CUDA graph" if e2e_graph is not None else "")),
+                "graph": e2e_graph is not None},
         "gpu_launches": K * step.launches_per_step,
         "clocks": clk,
         "cpu_baseline": cpu,
