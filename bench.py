@@ -633,7 +633,7 @@ def run_ours(args):
     achieved = step.attn_alg_bytes / (attn_avg_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(step.inp, spec, budget_s=args.cpu_budget)
     kern = {"v1": "paged_attention_decode", "v2_fixed": "paged_attention_v2_partition",
             "v2_splits": "paged_attention_v2_partition"}[step.mode]
