@@ -122,7 +122,8 @@ size_t pkv_decode_args_size(void);
 /*
  * Tuning knob for paged_attention_decode / paged_attention_v2_partition: warps
  * per CTA, i.e. how many warps split one (sequence, kv head, partition) unit.
- * 0 (default) picks per call from the number of units and the SM count;
+ * 0 (default) picks per call from the pass (single or split), the number of
+ * units and the SM count (see the launcher for the measured rule);
  * 1, 2 or 4 forces that value where the instance exists.  Process-wide.
  * Returns PKV_ERR_INVALID_ARG for any other value.
  */

@@ -115,16 +115,28 @@ AttnParams make_params(const pkv_decode_args_t *a) {
   return p;
 }
 
-// Warps per CTA: one warp per work unit when there are enough units to fill
-// every SM several times over, four (splitting the unit's chunks) otherwise.
-int pick_warps(const pkv_decode_args_t *a, int64_t units) {
+// Warps per CTA, from measurements on GB300 (the instance must exist):
+// - single pass: 4 (a unit is a whole sequence; more warps per CTA shorten
+//   the tail of long sequences, at any batch size measured);
+// - split-KV with enough units to fill every SM many times over: 1 for fixed
+//   partitions of at most 512 tokens (short, even units), 2 for split counts
+//   or longer partitions (units can be long and uneven);
+// - split-KV with few units: 4.
+enum class Pass { kSingle, kFixed, kSplits };
+
+int pick_warps(const pkv_decode_args_t *a, int64_t units, Pass pass, int partition_size) {
   const int forced = g_forced_warps.load(std::memory_order_relaxed);
-  if (forced == 1 || forced == 2 || forced == 4) {
-    if (smem_for(a->dtype, a->head_size, a->block_size, forced) != 0) return forced;
-  }
-  const bool four_ok = smem_for(a->dtype, a->head_size, a->block_size, 4) != 0;
-  if (!four_ok) return 1;
-  return units >= int64_t(sm_count()) * 16 ? 1 : 4;
+  auto have = [&](int w) { return smem_for(a->dtype, a->head_size, a->block_size, w) != 0; };
+  if ((forced == 1 || forced == 2 || forced == 4) && have(forced)) return forced;
+  int want;
+  if (pass == Pass::kSingle || units < int64_t(sm_count()) * 16)
+    want = 4;
+  else if (pass == Pass::kFixed && partition_size <= 512)
+    want = 1;
+  else
+    want = 2;
+  while (want > 1 && !have(want)) want /= 2;
+  return want;
 }
 
 }  // namespace
@@ -179,7 +191,7 @@ pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
   p.o_s2 = out_stride[2];
   p.max_parts = 1;
   dim3 grid(1, args->num_kv_heads, args->num_seqs);
-  const int w = pick_warps(args, int64_t(args->num_kv_heads) * args->num_seqs);
+  const int w = pick_warps(args, int64_t(args->num_kv_heads) * args->num_seqs, Pass::kSingle, 0);
   return pkv::launch_attention(args->dtype, p, args->head_size, args->block_size, w, grid,
                                reinterpret_cast<cudaStream_t>(stream));
 }
@@ -211,7 +223,8 @@ pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float
   p.splits = num_kv_splits;
   dim3 grid(max_num_partitions, args->num_kv_heads, args->num_seqs);
   const int64_t units = int64_t(max_num_partitions) * args->num_kv_heads * args->num_seqs;
-  const int w = pick_warps(args, units);
+  const int w = pick_warps(args, units, num_kv_splits ? Pass::kSplits : Pass::kFixed,
+                           partition_size);
   return pkv::launch_attention(args->dtype, p, args->head_size, args->block_size, w, grid,
                                reinterpret_cast<cudaStream_t>(stream));
 }
