@@ -161,7 +161,9 @@ pkv_status_t pkv_test_set_unarrived_bytes(uint32_t bytes);
  *   out: [num_seqs, num_heads, head_size] in args->dtype with strides out_stride.
  *   A sequence with seq_len == 0 gets a zero output row.
  * Supported: fp16/bf16 with head_size in {64, 128, 256}; fp32 with head_size in
- * {64, 128}; block_size in {8, 16, 32}; num_heads/num_kv_heads <= 8.
+ * {64, 128}; block_size in {8, 16, 32}; any num_heads/num_kv_heads (a kv head's
+ * query heads are served 8 at a time; above 8 its pages are read once per 8
+ * heads, mostly from L2), with num_kv_heads * ceil(group / 8) <= 65535.
  */
 pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
                                     const pkv_decode_args_t *args, pkv_stream_t stream);

@@ -68,8 +68,10 @@ pkv_status_t check_decode_args(const pkv_decode_args_t *a) {
   if (a->block_size < 1 || a->max_blocks_per_seq < 0 || a->num_blocks < 1)
     return PKV_ERR_INVALID_ARG;
   if (!std::isfinite(a->scale)) return PKV_ERR_INVALID_ARG;
-  if (a->num_seqs > 65535 || a->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
-  if (a->num_heads / a->num_kv_heads > pkv::kMaxGroup) return PKV_ERR_UNSUPPORTED;
+  const int64_t head_groups =
+      (a->num_heads / a->num_kv_heads + pkv::kMaxGroup - 1) / pkv::kMaxGroup;
+  if (a->num_seqs > 65535 || int64_t(a->num_kv_heads) * head_groups > 65535)
+    return PKV_ERR_UNSUPPORTED;
   if (smem_for(a->dtype, a->head_size, a->block_size, 1) == 0) return PKV_ERR_UNSUPPORTED;
   if (a->num_seqs == 0) return PKV_OK;
   if (!a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->seq_lens)
@@ -107,6 +109,7 @@ AttnParams make_params(const pkv_decode_args_t *a) {
   p.num_heads = a->num_heads;
   p.num_kv_heads = a->num_kv_heads;
   p.group = a->num_heads / a->num_kv_heads;
+  p.head_groups = (p.group + pkv::kMaxGroup - 1) / pkv::kMaxGroup;
   p.num_blocks = a->num_blocks;
   p.max_blocks_per_seq = a->max_blocks_per_seq;
   p.scale_log2 = a->scale * 1.44269504088896340736f;
@@ -190,8 +193,8 @@ pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
   p.o_s1 = out_stride[1];
   p.o_s2 = out_stride[2];
   p.max_parts = 1;
-  dim3 grid(1, args->num_kv_heads, args->num_seqs);
-  const int w = pick_warps(args, int64_t(args->num_kv_heads) * args->num_seqs, Pass::kSingle, 0);
+  dim3 grid(1, args->num_kv_heads * p.head_groups, args->num_seqs);
+  const int w = pick_warps(args, int64_t(grid.y) * args->num_seqs, Pass::kSingle, 0);
   return pkv::launch_attention(args->dtype, p, args->head_size, args->block_size, w, grid,
                                reinterpret_cast<cudaStream_t>(stream));
 }
@@ -221,8 +224,8 @@ pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float
   p.max_parts = max_num_partitions;
   p.partition_size = num_kv_splits ? 0 : partition_size;
   p.splits = num_kv_splits;
-  dim3 grid(max_num_partitions, args->num_kv_heads, args->num_seqs);
-  const int64_t units = int64_t(max_num_partitions) * args->num_kv_heads * args->num_seqs;
+  dim3 grid(max_num_partitions, args->num_kv_heads * p.head_groups, args->num_seqs);
+  const int64_t units = int64_t(max_num_partitions) * grid.y * args->num_seqs;
   const int w = pick_warps(args, units, num_kv_splits ? Pass::kSplits : Pass::kFixed,
                            partition_size);
   return pkv::launch_attention(args->dtype, p, args->head_size, args->block_size, w, grid,

@@ -54,6 +54,7 @@ struct AttnParams {
   const int32_t *seq_lens;
   int32_t *err;
   int32_t num_heads, num_kv_heads, group, num_blocks, max_blocks_per_seq;
+  int32_t head_groups;  // ceil(group / kMaxGroup): CTAs per kv head along grid y
   float scale_log2;  // scale * log2(e)
   int32_t mode;
   void *out;  // v1 output
@@ -103,12 +104,16 @@ __global__ void __launch_bounds__(WARPS * 32)
   constexpr int NST = Cfg::kStages;
   constexpr unsigned FULL = 0xffffffffu;
 
+  // Grid y enumerates (kv head, sub-group): a kv head with more than kMaxGroup
+  // query heads is served by several CTAs, each taking up to kMaxGroup of them
+  // (their page reads after the first mostly hit L2).
   const int part = blockIdx.x;
-  const int kvh = blockIdx.y;
+  const int kvh = int(blockIdx.y) / p.head_groups;
+  const int hsub = int(blockIdx.y) - kvh * p.head_groups;
   const int seq = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = p.group;
+  const int g = min(kMaxGroup, p.group - hsub * kMaxGroup);  // query heads of this CTA
   const bool leader = threadIdx.x == 0;
   grid_dependency_wait();
   allow_dependent_launch();
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     t1 = part < n ? min(t0 + c, int64_t(L)) : t0;
   }
 
-  const int h0 = kvh * g;
+  const int h0 = kvh * p.group + hsub * kMaxGroup;
   if (t0 >= t1) {
     if (p.mode == kModeV1) {
       T *out = static_cast<T *>(p.out);

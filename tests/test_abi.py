@@ -88,7 +88,7 @@ def _decode(lib, a, out=0x3000):
     ("x", 4, 1),                # x * sizeof(bf16) != 16
     ("head_size", 96, 2),       # not built
     ("block_size", 24, 2),      # not built
-    ("num_kv_heads", 1, 1),     # 8 / 1 = group 8 is fine but head check below
+    ("num_kv_heads", 1, 1),     # grid limit on kv heads x query-head sub-groups (below)
     ("query", None, 1),         # null pointer
     ("seq_lens", None, 1),
     ("num_blocks", 0, 1),
@@ -97,7 +97,7 @@ def _decode(lib, a, out=0x3000):
 ])
 def test_decode_rejects_bad_arguments(lib, field, value, status):
     if field == "num_kv_heads":
-        a = _args(num_heads=32, num_kv_heads=2)  # group 16 > 8: not built
+        a = _args(num_heads=40000 * 9, num_kv_heads=40000)  # 40000 kv heads x 2 sub-groups
         assert _decode(lib, a) == 2
         return
     a = _args(**{field: value})

@@ -313,3 +313,22 @@ def test_copy_wait_timeout_is_reported_and_the_context_survives():
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         assert_attention_close(out, _oracle_v1(inp), DT[dtype], f"after timeout {dtype}")
+
+
+@pytest.mark.parametrize("dtype,D,bs,H,Hk", [("bf16", 128, 16, 16, 1), ("bf16", 128, 16, 128, 8),
+                                             ("f16", 64, 8, 18, 2), ("bf16", 256, 32, 64, 2),
+                                             ("f32", 64, 16, 32, 1), ("bf16", 128, 16, 64, 1)])
+def test_groups_larger_than_eight(dtype, D, bs, H, Hk):
+    """A kv head serving 9..64 query heads (sub-groups of 8 per CTA): single
+    pass, fixed partitions and split counts all match the oracle."""
+    lens = [1, 300, 1025, 17]
+    inp = _inputs(dtype, D, bs, H, Hk, lens, seed=H + Hk + D, peaky_fraction=0.01)
+    g = on_device(inp)
+    ref = _oracle_v1(inp)
+    assert_attention_close(run_v1(g), ref, DT[dtype], f"v1 {H}/{Hk}")
+    maxP = -(-inp["max_blocks_per_seq"] * bs // 128)
+    _, _, _, out = run_v2(g, maxP, partition_size=128)
+    assert_attention_close(out, ref, DT[dtype], f"v2 fixed {H}/{Hk}")
+    splits = torch.tensor([1, 2, 3, 1], dtype=torch.int32, device="cuda")
+    _, _, _, out = run_v2(g, 4, splits=splits)
+    assert_attention_close(out, ref, DT[dtype], f"v2 splits {H}/{Hk}")
