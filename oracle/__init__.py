@@ -5,7 +5,9 @@ computes.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
 baseline leg may import it; the CUDA library shares no code with it and never
 calls it.  Each function cites the passage of the pages it follows.
 """
+from . import fp8  # noqa: F401
 from .attention import (  # noqa: F401
+    alibi_bias,
     attention_one_head,
     decode_v1,
     gather_kv,

@@ -23,7 +23,13 @@ decode kernels reach faster, step by step as the pages state it:
   (``_paged_attn_v2_reduce_kernel``: global max, rescale, weighted sum).
 
 Everything is upcast to float64 from the exact stored values before any
-arithmetic.  The query-head -> kv-head map is ``h // (num_heads //
+arithmetic.
+
+Two variants the same page's wrapper names but does not define
+(``alibi_slopes``, ``kv_cache_dtype`` / ``k_scale`` / ``v_scale``), in the
+reading stated in ``oracle.fp8`` and ``alibi_bias``: fp8 caches are decoded
+from their 8-bit codes and scaled, and ALiBi adds ``slope_h * (t - L + 1)``
+to the logit of token ``t``.  The query-head -> kv-head map is ``h // (num_heads //
 num_kv_heads)`` (contiguous groups, the vLLM convention the page says it
 follows; its own mapping line is a placeholder marked TODO).
 """
@@ -32,6 +38,8 @@ from __future__ import annotations
 from typing import Optional, Sequence, Tuple
 
 import torch
+
+from . import fp8
 
 __all__ = [
     "token_offsets",
@@ -44,6 +52,7 @@ __all__ = [
     "partition_ranges",
     "v2_partition",
     "v2_reduce",
+    "alibi_bias",
 ]
 
 NEG_INF = float("-inf")
@@ -82,11 +91,14 @@ def sequence_block_ids(block_tables: torch.Tensor, seq: int, num_pages: int,
 
 
 def gather_kv(key_cache: torch.Tensor, value_cache: torch.Tensor, block_ids: torch.Tensor,
-              seq_len: int, kv_head: int) -> Tuple[torch.Tensor, torch.Tensor]:
+              seq_len: int, kv_head: int, kv_format: Optional[str] = None, k_scale: float = 1.0,
+              v_scale: float = 1.0) -> Tuple[torch.Tensor, torch.Tensor]:
     """Materialise one sequence's keys and values, ``[seq_len, head_size]`` float64.
 
     ``k_t[d] = key_cache[b, kv_head, d // x, t % bs, d % x]`` and
     ``v_t[d] = value_cache[b, kv_head, d, t % bs]`` with ``b = block_ids[t // bs]``.
+    With an fp8 ``kv_format`` the caches hold uint8 codes: keys are
+    ``decode(code) * k_scale`` and values ``decode(code) * v_scale``.
     """
     bs = key_cache.shape[3]
     D = value_cache.shape[2]
@@ -95,20 +107,53 @@ def gather_kv(key_cache: torch.Tensor, value_cache: torch.Tensor, block_ids: tor
     slot = t % bs
     # Advanced indices (blk, kv_head, slot) are separated by a slice, so the
     # token axis comes first: [seq_len, head_size // x, x] and [seq_len, head_size].
-    K = key_cache[blk, kv_head, :, slot, :].to(torch.float64).reshape(seq_len, D)
-    V = value_cache[blk, kv_head, :, slot].to(torch.float64)
-    return K, V
+    K = key_cache[blk, kv_head, :, slot, :].reshape(seq_len, D)
+    V = value_cache[blk, kv_head, :, slot]
+    if kv_format is None:
+        return K.to(torch.float64), V.to(torch.float64)
+    return fp8.decode(K, kv_format) * k_scale, fp8.decode(V, kv_format) * v_scale
 
 
-def attention_one_head(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float):
+def alibi_bias(slope: float, seq_len: int) -> torch.Tensor:
+    """ALiBi term of every logit of one decode query, ``[seq_len]`` float64.
+
+    The split-KV wrapper on page "paged_attention_v2_triton.py" takes
+    ``alibi_slopes`` without defining them.  Reading: ALiBi as defined in
+    "Train Short, Test Long: Attention with Linear Biases" (Press, Smith,
+    Lewis, 2022), a bias of ``-slope * distance`` between the query and key
+    positions, with the decode query at position ``seq_len - 1``:
+    ``slope * (t - seq_len + 1)`` for key ``t``, added to the scaled score.
+    """
+    t = torch.arange(seq_len, dtype=torch.float64)
+    return float(slope) * (t - (seq_len - 1))
+
+
+def _kv_options(key_cache, value_cache, kv_cache_dtype, k_scale, v_scale):
+    """(caches as stored codes, keyword arguments for gather_kv)."""
+    fmt = fp8.format_of(kv_cache_dtype)
+    if fmt is None:
+        return key_cache, value_cache, {}
+    if key_cache.dtype != torch.uint8:
+        key_cache = key_cache.view(torch.uint8)
+    if value_cache.dtype != torch.uint8:
+        value_cache = value_cache.view(torch.uint8)
+    return key_cache, value_cache, dict(kv_format=fmt, k_scale=float(k_scale),
+                                        v_scale=float(v_scale))
+
+
+def attention_one_head(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float,
+                       bias: Optional[torch.Tensor] = None):
     """Textbook softmax attention of one query vector over ``K``/``V`` (float64).
 
+    ``bias`` (optional, ``[seq_len]``) is added to the scaled scores.
     Returns ``(out, logits)``; an empty sequence gives a zero output.
     """
     q = q.to(torch.float64)
     if K.shape[0] == 0:
         return torch.zeros(V.shape[1], dtype=torch.float64), torch.zeros(0, dtype=torch.float64)
     z = (K @ q) * scale
+    if bias is not None:
+        z = z + bias
     p = torch.exp(z - z.max())
     p = p / p.sum()
     return p @ V, z
@@ -124,15 +169,21 @@ def kv_head_of(head: int, num_heads: int, num_kv_heads: int) -> int:
 
 def decode_v1(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
               seqs: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None,
-              kv_indptr: Optional[torch.Tensor] = None) -> torch.Tensor:
+              kv_indptr: Optional[torch.Tensor] = None, kv_cache_dtype: str = "auto",
+              k_scale: float = 1.0, v_scale: float = 1.0,
+              alibi_slopes: Optional[Sequence[float]] = None) -> torch.Tensor:
     """Single-pass decode output ``[num_seqs, num_heads, head_size]`` float64.
 
     ``seqs`` / ``heads`` restrict the work to a subset (other rows stay NaN),
     so that full-size batches can be checked on sampled outputs.
+    ``kv_cache_dtype`` / ``k_scale`` / ``v_scale``: see ``oracle.fp8``;
+    ``alibi_slopes`` (``[num_heads]``): see ``alibi_bias``.
     """
     B, H, D = query.shape
     Hk = key_cache.shape[1]
     bs = key_cache.shape[3]
+    key_cache, value_cache, kvq = _kv_options(key_cache, value_cache, kv_cache_dtype, k_scale,
+                                              v_scale)
     out = torch.full((B, H, D), float("nan"), dtype=torch.float64)
     seqs = range(B) if seqs is None else seqs
     heads = range(H) if heads is None else heads
@@ -143,9 +194,10 @@ def decode_v1(query, key_cache, value_cache, block_tables, seq_lens, scale: floa
         for h in heads:
             kvh = kv_head_of(h, H, Hk)
             if kvh not in cache:
-                cache[kvh] = gather_kv(key_cache, value_cache, ids, L, kvh)
+                cache[kvh] = gather_kv(key_cache, value_cache, ids, L, kvh, **kvq)
             K, V = cache[kvh]
-            out[s, h], _ = attention_one_head(query[s, h], K, V, scale)
+            bias = None if alibi_slopes is None else alibi_bias(float(alibi_slopes[h]), L)
+            out[s, h], _ = attention_one_head(query[s, h], K, V, scale, bias)
     return out
 
 
@@ -191,7 +243,9 @@ def v2_partition(query, key_cache, value_cache, block_tables, seq_lens, scale: f
                  max_num_partitions: int, partition_size: Optional[int] = None,
                  num_kv_splits: Optional[Sequence[int]] = None,
                  seqs: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None,
-                 kv_indptr: Optional[torch.Tensor] = None):
+                 kv_indptr: Optional[torch.Tensor] = None, kv_cache_dtype: str = "auto",
+                 k_scale: float = 1.0, v_scale: float = 1.0,
+                 alibi_slopes: Optional[Sequence[float]] = None):
     """Per-partition statistics of split-KV decode, all float64.
 
     Returns ``tmp_output [B, H, maxP, D]``, ``exp_sums [B, H, maxP]`` and
@@ -199,11 +253,15 @@ def v2_partition(query, key_cache, value_cache, block_tables, seq_lens, scale: f
     tokens: ``max_logits = max z``, ``exp_sums = sum exp(z - max)`` and
     ``tmp_output = sum exp(z - max) v / exp_sums`` (normalised: that is what
     the page's reduce weights assume).  Empty partitions hold ``-inf`` / ``0``
-    and a NaN ``tmp_output`` row (the kernels leave it untouched).
+    and a NaN ``tmp_output`` row (the kernels leave it untouched).  The
+    logits include the ALiBi term when ``alibi_slopes`` is given, and fp8
+    caches are decoded as in ``decode_v1``.
     """
     B, H, D = query.shape
     Hk = key_cache.shape[1]
     bs = key_cache.shape[3]
+    key_cache, value_cache, kvq = _kv_options(key_cache, value_cache, kv_cache_dtype, k_scale,
+                                              v_scale)
     tmp = torch.full((B, H, max_num_partitions, D), float("nan"), dtype=torch.float64)
     es = torch.full((B, H, max_num_partitions), float("nan"), dtype=torch.float64)
     ml = torch.full((B, H, max_num_partitions), float("nan"), dtype=torch.float64)
@@ -219,9 +277,11 @@ def v2_partition(query, key_cache, value_cache, block_tables, seq_lens, scale: f
         for h in heads:
             kvh = kv_head_of(h, H, Hk)
             if kvh not in cache:
-                cache[kvh] = gather_kv(key_cache, value_cache, ids, L, kvh)
+                cache[kvh] = gather_kv(key_cache, value_cache, ids, L, kvh, **kvq)
             K, V = cache[kvh]
             z = (K @ query[s, h].to(torch.float64)) * scale if L else torch.zeros(0, dtype=torch.float64)
+            if alibi_slopes is not None:
+                z = z + alibi_bias(float(alibi_slopes[h]), L)
             for p, (a, b) in enumerate(ranges):
                 if a >= b:
                     ml[s, h, p] = NEG_INF

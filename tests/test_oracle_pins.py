@@ -475,7 +475,7 @@ def test_pins_catch_planted_mistakes(monkeypatch):
 
     # 6. softmax without the max subtraction is still exact here, but a
     #    dropped normalisation is not
-    def bad_attention(q, K, V, scale):
+    def bad_attention(q, K, V, scale, bias=None):
         z = (K @ q.to(torch.float64)) * scale
         p = torch.exp(z - z.max())
         return p @ V, z
