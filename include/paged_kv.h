@@ -53,6 +53,20 @@ typedef struct CUstream_st *pkv_stream_t;
 
 typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype_t;
 
+/*
+ * Element format of key_cache / value_cache (pkv_decode_args_t.kv_cache_dtype).
+ * The page "paged_attention_v2_triton.py" (wrapper paged_attention_v2_triton,
+ * arguments kv_cache_dtype, k_scale, v_scale) names these without defining
+ * them; this library takes vLLM's reading:
+ *   PKV_KV_AUTO      caches hold `dtype` elements; k_scale / v_scale ignored.
+ *   PKV_KV_FP8_E4M3  caches hold one-byte OCP E4M3 codes ("fp8", "fp8_e4m3"):
+ *   PKV_KV_FP8_E5M2  or E5M2 codes ("fp8_e5m2"); x = 16 and a key element
+ *                    stands for decode(code) * k_scale, a value element for
+ *                    decode(code) * v_scale.  Queries and the output stay in
+ *                    `dtype`, which must then be PKV_F16 or PKV_BF16.
+ */
+typedef enum { PKV_KV_AUTO = 0, PKV_KV_FP8_E4M3 = 1, PKV_KV_FP8_E5M2 = 2 } pkv_kv_cache_dtype_t;
+
 typedef enum {
   PKV_OK = 0,
   PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent strides */
@@ -87,6 +101,16 @@ typedef enum {
  *       kv_indptr[s+1]-kv_indptr[s] pages available to it.
  *   seq_lens: [num_seqs] int32 context lengths.
  *   err_flag: optional device int32 receiving PKV_ERRF_* bits.
+ *   kv_cache_dtype, k_scale, v_scale: cache element format (pkv_kv_cache_dtype_t
+ *       above); a zero-initialised struct means PKV_KV_AUTO.  With fp8 the
+ *       scales must be finite; x, the key/value strides and the 16-byte rules
+ *       count one-byte elements.
+ *   alibi_slopes: optional [num_heads] fp32 device array (4-byte aligned).
+ *       Non-NULL adds slope[h] * (t - seq_len + 1) to the scaled score of
+ *       query head h and token t: ALiBi ("Train Short, Test Long", Press et
+ *       al.) with the decode query at position seq_len - 1, the reading of the
+ *       alibi_slopes argument the page "paged_attention_v2_triton.py" names.
+ *       It enters max_logits of the split-KV pass like any logit.
  */
 typedef struct {
   int32_t num_seqs;
@@ -110,6 +134,10 @@ typedef struct {
   const int32_t *kv_indptr;
   const int32_t *seq_lens;
   int32_t *err_flag;
+  int32_t kv_cache_dtype; /* pkv_kv_cache_dtype_t */
+  float k_scale;
+  float v_scale;
+  const float *alibi_slopes;
 } pkv_decode_args_t;
 
 /* Library version string, e.g. "paged_kv 0.1.0 sm_103a". */
@@ -164,6 +192,9 @@ pkv_status_t pkv_test_set_unarrived_bytes(uint32_t bytes);
  * {64, 128}; block_size in {8, 16, 32}; any num_heads/num_kv_heads (a kv head's
  * query heads are served 8 at a time; above 8 its pages are read once per 8
  * heads, mostly from L2), with num_kv_heads * ceil(group / 8) <= 65535.
+ * fp8 caches (kv_cache_dtype != PKV_KV_AUTO): fp16/bf16 queries, the same head
+ * and block sizes.  With alibi_slopes the logit of token t gains the ALiBi
+ * term described at pkv_decode_args_t.
  */
 pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
                                     const pkv_decode_args_t *args, pkv_stream_t stream);

@@ -46,6 +46,11 @@ PKV_ERRF_BLOCK_ID, PKV_ERRF_SEQ_LEN, PKV_ERRF_SPLITS, PKV_ERRF_INDPTR, PKV_ERRF_
 
 _DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
+# kv_cache_dtype names (vLLM's) -> pkv_kv_cache_dtype_t
+_KV_CACHE_CODE = {"auto": 0, "fp8": 1, "fp8_e4m3": 1, "fp8_e5m2": 2}
+_FP8_TORCH = {getattr(torch, n): c for n, c in (("float8_e4m3fn", 1), ("float8_e5m2", 2))
+              if hasattr(torch, n)}
+
 _c_i32, _c_i64, _c_f32, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 _I64x3 = _c_i64 * 3
 
@@ -63,6 +68,8 @@ class DecodeArgs(ctypes.Structure):
         ("value_cache", _c_p), ("v_stride", _c_i64 * 4),
         ("block_tables", _c_p), ("bt_stride", _c_i64 * 2),
         ("kv_indptr", _c_p), ("seq_lens", _c_p), ("err_flag", _c_p),
+        ("kv_cache_dtype", _c_i32), ("k_scale", _c_f32), ("v_scale", _c_f32),
+        ("alibi_slopes", _c_p),
     ]
 
 
@@ -214,16 +221,43 @@ def _test_set_unarrived_bytes(nbytes: int) -> None:
     _check(lib().pkv_test_set_unarrived_bytes(int(nbytes)), "pkv_test_set_unarrived_bytes")
 
 
+def _kv_cache_code(key_cache, value_cache, query, kv_cache_dtype) -> int:
+    """pkv_kv_cache_dtype_t of the caches.  fp8 caches are uint8 tensors of
+    codes with an explicit ``kv_cache_dtype`` ("fp8", "fp8_e4m3", "fp8_e5m2"),
+    or float8_e4m3fn / float8_e5m2 tensors ("auto" reads the format from them)."""
+    if kv_cache_dtype not in _KV_CACHE_CODE:
+        raise ValueError(f"unknown kv_cache_dtype {kv_cache_dtype!r}")
+    if key_cache.dtype != value_cache.dtype:
+        raise ValueError("key_cache and value_cache must share a dtype")
+    code = _KV_CACHE_CODE[kv_cache_dtype]
+    if key_cache.dtype in _FP8_TORCH:
+        if code not in (0, _FP8_TORCH[key_cache.dtype]):
+            raise ValueError(f"kv_cache_dtype {kv_cache_dtype!r} contradicts {key_cache.dtype}")
+        return _FP8_TORCH[key_cache.dtype]
+    if code == 0:
+        if key_cache.dtype != query.dtype:
+            raise ValueError("query, key_cache and value_cache must share a dtype")
+        return 0
+    if key_cache.dtype != torch.uint8:
+        raise ValueError("fp8 caches are uint8 (codes) or float8 tensors")
+    return code
+
+
 def _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
-                 err_flag, max_blocks_per_seq) -> DecodeArgs:
+                 err_flag, max_blocks_per_seq, kv_cache_dtype="auto", k_scale=1.0, v_scale=1.0,
+                 alibi_slopes=None) -> DecodeArgs:
     for t, n in ((query, "query"), (key_cache, "key_cache"), (value_cache, "value_cache"),
                  (block_tables, "block_tables"), (seq_lens, "seq_lens"),
-                 (kv_indptr, "kv_indptr"), (err_flag, "err_flag")):
+                 (kv_indptr, "kv_indptr"), (err_flag, "err_flag"),
+                 (alibi_slopes, "alibi_slopes")):
         _cuda(t, n)
     if query.dtype not in _DTYPE_CODE:
         raise ValueError(f"unsupported dtype {query.dtype}")
-    if key_cache.dtype != query.dtype or value_cache.dtype != query.dtype:
-        raise ValueError("query, key_cache and value_cache must share a dtype")
+    kv_code = _kv_cache_code(key_cache, value_cache, query, kv_cache_dtype)
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or
+                                     not alibi_slopes.is_contiguous() or
+                                     tuple(alibi_slopes.shape) != (query.shape[1],)):
+        raise ValueError("alibi_slopes must be a contiguous float32 [num_heads] tensor")
     for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (kv_indptr, "kv_indptr"),
                  (err_flag, "err_flag")):
         if t is not None and t.dtype != torch.int32:
@@ -261,6 +295,10 @@ def _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, k
     a.kv_indptr = _ptr(kv_indptr)
     a.seq_lens = _ptr(seq_lens)
     a.err_flag = _ptr(err_flag)
+    a.kv_cache_dtype = kv_code
+    a.k_scale = float(k_scale)
+    a.v_scale = float(v_scale)
+    a.alibi_slopes = _ptr(alibi_slopes)
     return a
 
 
@@ -269,13 +307,17 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
                            seq_lens: torch.Tensor, scale: float, *,
                            kv_indptr: Optional[torch.Tensor] = None,
                            err_flag: Optional[torch.Tensor] = None,
-                           max_blocks_per_seq: Optional[int] = None, stream=None) -> None:
+                           max_blocks_per_seq: Optional[int] = None,
+                           kv_cache_dtype: str = "auto", k_scale: float = 1.0,
+                           v_scale: float = 1.0, alibi_slopes: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
     """Single-pass decode into ``out [num_seqs, num_heads, head_size]`` (query's dtype)."""
     _cuda(out, "out")
     if out.dtype != query.dtype or tuple(out.shape) != tuple(query.shape):
         raise ValueError("out must match query's shape and dtype")
     a = _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
-                     err_flag, max_blocks_per_seq)
+                     err_flag, max_blocks_per_seq, kv_cache_dtype, k_scale,
+                     v_scale, alibi_slopes)
     os_ = _I64x3(*out.stride())
     _check(lib().paged_attention_decode(_ptr(out), os_, ctypes.byref(a), _stream(stream)),
            "paged_attention_decode")
@@ -289,7 +331,10 @@ def paged_attention_v2_partition(tmp_out: torch.Tensor, exp_sums: torch.Tensor,
                                  num_kv_splits: Optional[torch.Tensor] = None,
                                  kv_indptr: Optional[torch.Tensor] = None,
                                  err_flag: Optional[torch.Tensor] = None,
-                                 max_blocks_per_seq: Optional[int] = None, stream=None) -> None:
+                                 max_blocks_per_seq: Optional[int] = None,
+                                 kv_cache_dtype: str = "auto", k_scale: float = 1.0,
+                                 v_scale: float = 1.0, alibi_slopes: Optional[torch.Tensor] = None,
+                                 stream=None) -> None:
     """Split-KV partition pass; ``tmp_out [B,H,maxP,D]``, ``exp_sums``/``max_logits [B,H,maxP]`` fp32."""
     for t, n in ((tmp_out, "tmp_out"), (exp_sums, "exp_sums"), (max_logits, "max_logits"),
                  (num_kv_splits, "num_kv_splits")):
@@ -304,7 +349,8 @@ def paged_attention_v2_partition(tmp_out: torch.Tensor, exp_sums: torch.Tensor,
     if num_kv_splits is not None and num_kv_splits.dtype != torch.int32:
         raise ValueError("num_kv_splits must be int32")
     a = _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
-                     err_flag, max_blocks_per_seq)
+                     err_flag, max_blocks_per_seq, kv_cache_dtype, k_scale,
+                     v_scale, alibi_slopes)
     _check(lib().paged_attention_v2_partition(_ptr(tmp_out), _ptr(exp_sums), _ptr(max_logits),
                                               maxP, int(partition_size), _ptr(num_kv_splits),
                                               ctypes.byref(a), _stream(stream)),
@@ -516,7 +562,10 @@ def paged_attention_v2_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache
                                num_kv_splits: Optional[torch.Tensor] = None,
                                kv_indptr: Optional[torch.Tensor] = None,
                                err_flag: Optional[torch.Tensor] = None,
-                               max_blocks_per_seq: Optional[int] = None, stream=None) -> None:
+                               max_blocks_per_seq: Optional[int] = None,
+                               kv_cache_dtype: str = "auto", k_scale: float = 1.0,
+                               v_scale: float = 1.0, alibi_slopes: Optional[torch.Tensor] = None,
+                               stream=None) -> None:
     """Split-KV decode into ``out`` for callers that cannot allocate device
     memory: the partition scratch lives in the library's fixed device array
     (see ``noalloc_scratch_bytes``) instead of caller-provided buffers.  Calls
@@ -528,7 +577,8 @@ def paged_attention_v2_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache
     if num_kv_splits is not None and num_kv_splits.dtype != torch.int32:
         raise ValueError("num_kv_splits must be int32")
     a = _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
-                     err_flag, max_blocks_per_seq)
+                     err_flag, max_blocks_per_seq, kv_cache_dtype, k_scale,
+                     v_scale, alibi_slopes)
     os_ = _I64x3(*out.stride())
     _check(lib().paged_attention_v2_noalloc(_ptr(out), os_, int(max_num_partitions),
                                             int(partition_size), _ptr(num_kv_splits),

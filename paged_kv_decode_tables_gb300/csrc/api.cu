@@ -47,11 +47,29 @@ bool stride_bytes16(int64_t stride, int elem) {
   return (b % 16) == 0;
 }
 
-size_t smem_for(pkv_dtype_t t, int D, int BS, int W) {
+bool is_fp8_cache(int32_t kv) { return kv == PKV_KV_FP8_E4M3 || kv == PKV_KV_FP8_E5M2; }
+
+// Bytes of one cache element.
+int cache_elem_size(const pkv_decode_args_t *a) {
+  return is_fp8_cache(a->kv_cache_dtype) ? 1 : elem_size(a->dtype);
+}
+
+size_t smem_for(pkv_dtype_t t, int32_t kv, int D, int BS, int W) {
+  if (kv == PKV_KV_AUTO) {
+    switch (t) {
+      case PKV_F32: return pkv::smem_attention_f32(D, BS, W);
+      case PKV_F16: return pkv::smem_attention_f16(D, BS, W);
+      case PKV_BF16: return pkv::smem_attention_bf16(D, BS, W);
+      default: return 0;
+    }
+  }
+  const bool e4m3 = kv == PKV_KV_FP8_E4M3;
   switch (t) {
-    case PKV_F32: return pkv::smem_attention_f32(D, BS, W);
-    case PKV_F16: return pkv::smem_attention_f16(D, BS, W);
-    case PKV_BF16: return pkv::smem_attention_bf16(D, BS, W);
+    case PKV_F16:
+      return e4m3 ? pkv::smem_attention_f16_e4m3(D, BS, W) : pkv::smem_attention_f16_e5m2(D, BS, W);
+    case PKV_BF16:
+      return e4m3 ? pkv::smem_attention_bf16_e4m3(D, BS, W)
+                  : pkv::smem_attention_bf16_e5m2(D, BS, W);
     default: return 0;
   }
 }
@@ -59,8 +77,15 @@ size_t smem_for(pkv_dtype_t t, int D, int BS, int W) {
 // Checks shared by decode and the v2 partition pass.
 pkv_status_t check_decode_args(const pkv_decode_args_t *a) {
   if (a == nullptr) return PKV_ERR_INVALID_ARG;
-  const int es = elem_size(a->dtype);
-  if (es == 0) return PKV_ERR_INVALID_ARG;
+  if (elem_size(a->dtype) == 0) return PKV_ERR_INVALID_ARG;
+  if (a->kv_cache_dtype != PKV_KV_AUTO && !is_fp8_cache(a->kv_cache_dtype))
+    return PKV_ERR_INVALID_ARG;
+  if (is_fp8_cache(a->kv_cache_dtype)) {
+    if (!std::isfinite(a->k_scale) || !std::isfinite(a->v_scale)) return PKV_ERR_INVALID_ARG;
+    if (a->dtype == PKV_F32) return PKV_ERR_UNSUPPORTED;
+  }
+  if ((reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u) != 0) return PKV_ERR_INVALID_ARG;
+  const int es = cache_elem_size(a);
   if (a->num_seqs < 0 || a->num_heads < 1 || a->num_kv_heads < 1) return PKV_ERR_INVALID_ARG;
   if (a->num_heads % a->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (a->x * es != 16) return PKV_ERR_INVALID_ARG;
@@ -72,7 +97,8 @@ pkv_status_t check_decode_args(const pkv_decode_args_t *a) {
       (a->num_heads / a->num_kv_heads + pkv::kMaxGroup - 1) / pkv::kMaxGroup;
   if (a->num_seqs > 65535 || int64_t(a->num_kv_heads) * head_groups > 65535)
     return PKV_ERR_UNSUPPORTED;
-  if (smem_for(a->dtype, a->head_size, a->block_size, 1) == 0) return PKV_ERR_UNSUPPORTED;
+  if (smem_for(a->dtype, a->kv_cache_dtype, a->head_size, a->block_size, 1) == 0)
+    return PKV_ERR_UNSUPPORTED;
   if (a->num_seqs == 0) return PKV_OK;
   if (!a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->seq_lens)
     return PKV_ERR_INVALID_ARG;
@@ -112,7 +138,10 @@ AttnParams make_params(const pkv_decode_args_t *a) {
   p.head_groups = (p.group + pkv::kMaxGroup - 1) / pkv::kMaxGroup;
   p.num_blocks = a->num_blocks;
   p.max_blocks_per_seq = a->max_blocks_per_seq;
-  p.scale_log2 = a->scale * 1.44269504088896340736f;
+  const bool fp8 = is_fp8_cache(a->kv_cache_dtype);
+  p.scale_log2 = (fp8 ? a->scale * a->k_scale : a->scale) * 1.44269504088896340736f;
+  p.out_scale = fp8 ? a->v_scale : 1.0f;
+  p.alibi = a->alibi_slopes;
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.extra_expect_tx = g_extra_expect_tx.load(std::memory_order_relaxed);
   return p;
@@ -129,7 +158,9 @@ enum class Pass { kSingle, kFixed, kSplits };
 
 int pick_warps(const pkv_decode_args_t *a, int64_t units, Pass pass, int partition_size) {
   const int forced = g_forced_warps.load(std::memory_order_relaxed);
-  auto have = [&](int w) { return smem_for(a->dtype, a->head_size, a->block_size, w) != 0; };
+  auto have = [&](int w) {
+    return smem_for(a->dtype, a->kv_cache_dtype, a->head_size, a->block_size, w) != 0;
+  };
   if ((forced == 1 || forced == 2 || forced == 4) && have(forced)) return forced;
   int want;
   if (pass == Pass::kSingle || units < int64_t(sm_count()) * 16)
@@ -195,7 +226,8 @@ pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
   p.max_parts = 1;
   dim3 grid(1, args->num_kv_heads * p.head_groups, args->num_seqs);
   const int w = pick_warps(args, int64_t(grid.y) * args->num_seqs, Pass::kSingle, 0);
-  return pkv::launch_attention(args->dtype, p, args->head_size, args->block_size, w, grid,
+  return pkv::launch_attention(args->dtype, pkv_kv_cache_dtype_t(args->kv_cache_dtype), p,
+                               args->head_size, args->block_size, w, grid,
                                reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -228,7 +260,8 @@ pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float
   const int64_t units = int64_t(max_num_partitions) * grid.y * args->num_seqs;
   const int w = pick_warps(args, units, num_kv_splits ? Pass::kSplits : Pass::kFixed,
                            partition_size);
-  return pkv::launch_attention(args->dtype, p, args->head_size, args->block_size, w, grid,
+  return pkv::launch_attention(args->dtype, pkv_kv_cache_dtype_t(args->kv_cache_dtype), p,
+                               args->head_size, args->block_size, w, grid,
                                reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -319,12 +352,26 @@ pkv_status_t prepare_decode_metadata(int32_t *page_indices, int64_t page_indices
 
 namespace pkv {
 
-pkv_status_t launch_attention(pkv_dtype_t dtype, const AttnParams &p, int head_size,
-                              int block_size, int warps, dim3 grid, cudaStream_t stream) {
+pkv_status_t launch_attention(pkv_dtype_t dtype, pkv_kv_cache_dtype_t kv, const AttnParams &p,
+                              int head_size, int block_size, int warps, dim3 grid,
+                              cudaStream_t stream) {
+  const int D = head_size, BS = block_size, W = warps;
+  if (kv == PKV_KV_AUTO) {
+    switch (dtype) {
+      case PKV_F32: return launch_attention_f32(p, D, BS, W, grid, stream);
+      case PKV_F16: return launch_attention_f16(p, D, BS, W, grid, stream);
+      case PKV_BF16: return launch_attention_bf16(p, D, BS, W, grid, stream);
+      default: return PKV_ERR_UNSUPPORTED;
+    }
+  }
+  const bool e4m3 = kv == PKV_KV_FP8_E4M3;
   switch (dtype) {
-    case PKV_F32: return launch_attention_f32(p, head_size, block_size, warps, grid, stream);
-    case PKV_F16: return launch_attention_f16(p, head_size, block_size, warps, grid, stream);
-    case PKV_BF16: return launch_attention_bf16(p, head_size, block_size, warps, grid, stream);
+    case PKV_F16:
+      return e4m3 ? launch_attention_f16_e4m3(p, D, BS, W, grid, stream)
+                  : launch_attention_f16_e5m2(p, D, BS, W, grid, stream);
+    case PKV_BF16:
+      return e4m3 ? launch_attention_bf16_e4m3(p, D, BS, W, grid, stream)
+                  : launch_attention_bf16_e5m2(p, D, BS, W, grid, stream);
     default: return PKV_ERR_UNSUPPORTED;
   }
 }

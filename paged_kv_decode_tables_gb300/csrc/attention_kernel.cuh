@@ -31,6 +31,22 @@
 // domain with ex2; row maxima use warp shuffles.
 //
 // fp32 runs the same pipeline with a CUDA-core body (no fp32 tensor path).
+//
+// fp8 caches (E4M3 / E5M2 codes, one byte per element; page
+// "paged_attention_v2_triton.py" names kv_cache_dtype, k_scale and v_scale in
+// its wrapper, read here as vLLM's dequantisation): the pages move as bytes,
+// half the traffic of a 16-bit cache, and each lane widens the codes it needs
+// to f16 in registers for the same f16 MMAs.  A 32-bit shared load returns 4
+// codes, so both products run on permuted index orders: the key row gives
+// dims 4j..4j+3 to the MMA's k-slots {2j, 2j+1, 2j+8, 2j+9} (the query
+// fragments use the same order), and the score rows hold the tile's tokens in
+// the order that puts tokens 4j..4j+3 on the value product's k-slots
+// {2j, 2j+1, 2j+8, 2j+9}.  bf16 queries go to f16 with a power-of-two scale
+// per head (max |q| lands in [2^14, 2^15)), taken back out of the logit
+// scale; k_scale joins the logit scale and v_scale the epilogue.
+//
+// ALiBi (optional slopes): the logit of token t gains slope_h * (t - L + 1),
+// added in the log2 domain as slope_h * log2(e) * (t - L + 1).
 #pragma once
 
 #include <type_traits>
@@ -64,18 +80,22 @@ struct AttnParams {
   const int32_t *splits;
   uint64_t wait_limit_ns;    // limit of every wait for a stage's copies
   uint32_t extra_expect_tx;  // test hook: bytes a stage expects that never arrive (0)
+  const float *alibi;        // [num_heads] ALiBi slopes, or null
+  float out_scale;           // multiplies the normalised output (v_scale for fp8 caches, else 1)
 };
 
 constexpr int kMaxGroup = 8;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
 
 __host__ __device__ constexpr int clamp_int(int v, int lo, int hi) {
   return v < lo ? lo : (v > hi ? hi : v);
 }
 
-template <typename T, int D, int BS, int WARPS>
+// KV is the cache element type: T itself, or an fp8 tag.
+template <typename KV, int D, int BS, int WARPS>
 struct AttnCfg {
-  static constexpr int kElem = int(sizeof(T));
+  static constexpr int kElem = int(sizeof(KV));
   static constexpr int kX = 16 / kElem;
   static constexpr int kChunk = BS >= 16 ? BS : 16;  // tokens per pipeline stage
   static constexpr int kPagesPerChunk = kChunk / BS;
@@ -94,11 +114,14 @@ struct AttnCfg {
   static_assert(kHalfStage % 16 == 0 && kPageBytes % 16 == 0, "bulk copies need 16 B");
 };
 
-template <typename T, int D, int BS, int WARPS>
+template <typename T, typename KV, int D, int BS, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
     paged_attention_kernel(const AttnParams p) {
-  using Cfg = AttnCfg<T, D, BS, WARPS>;
-  constexpr bool kMma = !std::is_same<T, float>::value;
+  using Cfg = AttnCfg<KV, D, BS, WARPS>;
+  constexpr bool kFp8 = is_fp8<KV>::value;
+  constexpr bool kMma = !std::is_same<T, float>::value && !kFp8;
+  static_assert(kFp8 || std::is_same<T, KV>::value, "a 16/32-bit cache has the query's type");
+  static_assert(!kFp8 || !std::is_same<T, float>::value, "fp8 caches take f16/bf16 queries");
   constexpr int PPC = Cfg::kPagesPerChunk;
   constexpr int CH = Cfg::kChunk;
   constexpr int NST = Cfg::kStages;
@@ -295,6 +318,16 @@ __global__ void __launch_bounds__(WARPS * 32)
         }
       }
     }
+    // ALiBi slopes (log2 units) of this lane's two score columns: heads
+    // 2*(lane%4) and 2*(lane%4)+1 of the CTA.
+    float sl2[2] = {0.f, 0.f};
+    if (p.alibi != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int h = 2 * (lane & 3) + j;
+        if (h < g) sl2[j] = p.alibi[h0 + h] * kLog2e;
+      }
+    }
     float acc[DT][4];
 #pragma unroll
     for (int dt = 0; dt < DT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
@@ -312,6 +345,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       waited = i + 1;
       const int64_t c = warp + int64_t(WARPS) * i;
       const int nv = int(min(int64_t(CH), t1 - (t0 + c * CH)));
+      const int pb = int(t0 + c * CH) - L + 1;  // ALiBi position of the chunk's token 0
       uint8_t *ks = wbase + st * Cfg::kStageBytes;
       uint8_t *vs = ks + Cfg::kHalfStage;
       if (nv < CH) {
@@ -348,7 +382,9 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int t = 16 * mt + (lane >> 2) + 8 * (e >> 1);
-          x[mt][e] = t < nv ? (s0[e] + s1[e]) * p.scale_log2 : -INFINITY;
+          float v = (s0[e] + s1[e]) * p.scale_log2;
+          if (p.alibi != nullptr) v = fmaf(sl2[e & 1], float(pb + t), v);
+          x[mt][e] = t < nv ? v : -INFINITY;
         }
       }
       float mloc[2] = {-INFINITY, -INFINITY};
@@ -444,6 +480,212 @@ __global__ void __launch_bounds__(WARPS * 32)
       epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
       epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
     }
+  } else if constexpr (kFp8) {
+    // ------------------------------------- fp8 cache, f16 tensor-core body --
+    constexpr int DT = D / 16;
+    const int gid = lane >> 2, tig = lane & 3;
+    // Query fragments (B operand, f16) of head gid: dims 16ks + 4tig + {0, 1}
+    // on k-slots 2tig, 2tig+1 and dims 16ks + 4tig + {2, 3} on 2tig+8, 2tig+9.
+    uint32_t qf[DT][2];
+    float head_unscale;  // 2^-k: undoes the f16 range scale 2^k of head gid's query
+    {
+      const T *qb = static_cast<const T *>(p.q) + int64_t(seq) * p.q_s0 +
+                    int64_t(h0 + gid) * p.q_s1;
+      float qv[DT][4];
+      float amax = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < DT; ++ks) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int d = 16 * ks + 4 * tig + j;
+          qv[ks][j] = gid < g ? to_f32<T>(qb[int64_t(d) * p.q_s2]) : 0.f;
+          amax = fmaxf(amax, fabsf(qv[ks][j]));
+        }
+      }
+      int k = 0;
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        // bf16 has f32's exponent range: bring max |q| into [2^14, 2^15) so
+        // every query element keeps its 8 significant bits in f16.
+        amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
+        if (amax > 0.f && amax < INFINITY)
+          k = clamp_int(141 - int(__float_as_uint(amax) >> 23), -120, 120);
+      }
+      const float up = __uint_as_float(uint32_t(127 + k) << 23);
+      head_unscale = __uint_as_float(uint32_t(127 - k) << 23);
+#pragma unroll
+      for (int ks = 0; ks < DT; ++ks) {
+        qf[ks][0] = pack2<__half>(qv[ks][0] * up, qv[ks][1] * up);
+        qf[ks][1] = pack2<__half>(qv[ks][2] * up, qv[ks][3] * up);
+      }
+    }
+    // Logit factor and ALiBi slope (log2 units) of this lane's two score
+    // columns, heads 2tig and 2tig+1 (head h's query is on lanes 4h..4h+3).
+    float xs2[2], sl2[2] = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = 2 * tig + j;
+      xs2[j] = p.scale_log2 * __shfl_sync(FULL, head_unscale, 4 * h);
+      if (p.alibi != nullptr && h < g) sl2[j] = p.alibi[h0 + h] * kLog2e;
+    }
+    float acc[DT][4];
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+
+    // Score row gid holds token rA of each 16-token tile, row gid+8 token rA+2,
+    // so that k-slots {2j, 2j+1, 2j+8, 2j+9} of the value product are tokens
+    // 4j..4j+3.
+    const int rA = 4 * (gid >> 1) + (gid & 1);
+    for (int i = 0; i < my_n; ++i) {
+      const int st = i % NST;
+      const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u, p.wait_limit_ns);
+      if (!__all_sync(FULL, got)) {
+        ok = false;
+        break;
+      }
+      waited = i + 1;
+      const int64_t c = warp + int64_t(WARPS) * i;
+      const int nv = int(min(int64_t(CH), t1 - (t0 + c * CH)));
+      const int pb = int(t0 + c * CH) - L + 1;  // ALiBi position of the chunk's token 0
+      uint8_t *ks = wbase + st * Cfg::kStageBytes;
+      uint8_t *vs = ks + Cfg::kHalfStage;
+      if (nv < CH) {
+        // Zero the value codes of tokens past the end (code 0 is +0).
+        const int ntail = CH - nv;
+        for (int e = lane; e < D * ntail; e += 32) {
+          const int d = e / ntail;
+          const int tau = nv + e % ntail;
+          vs[(tau / BS) * (D * BS) + d * BS + (tau % BS)] = 0;
+        }
+        __syncwarp();
+      }
+
+      float x[Cfg::kMTiles][4];
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int ta = 16 * mt + rA, tb = ta + 2;
+        const uint8_t *ka = ks + (ta / BS) * Cfg::kPageBytes + (ta % BS) * 16 + 4 * tig;
+        const uint8_t *kb = ks + (tb / BS) * Cfg::kPageBytes + (tb % BS) * 16 + 4 * tig;
+#pragma unroll
+        for (int k2 = 0; k2 < DT; ++k2) {
+          const uint32_t wa = *reinterpret_cast<const uint32_t *>(ka + k2 * (BS * 16));
+          const uint32_t wb = *reinterpret_cast<const uint32_t *>(kb + k2 * (BS * 16));
+          uint32_t a[4];
+          fp8x4_to_f16x2<KV>(wa, a[0], a[2]);
+          fp8x4_to_f16x2<KV>(wb, a[1], a[3]);
+          if (k2 & 1)
+            Mma16816<__half>::run(s1, a, qf[k2][0], qf[k2][1]);
+          else
+            Mma16816<__half>::run(s0, a, qf[k2][0], qf[k2][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 16 * mt + rA + 2 * (e >> 1);
+          float v = (s0[e] + s1[e]) * xs2[e & 1];
+          if (p.alibi != nullptr) v = fmaf(sl2[e & 1], float(pb + t), v);
+          x[mt][e] = t < nv ? v : -INFINITY;
+        }
+      }
+      float mloc[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        mloc[0] = fmaxf(mloc[0], fmaxf(x[mt][0], x[mt][2]));
+        mloc[1] = fmaxf(mloc[1], fmaxf(x[mt][1], x[mt][3]));
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mloc[0] = fmaxf(mloc[0], __shfl_xor_sync(FULL, mloc[0], o));
+        mloc[1] = fmaxf(mloc[1], __shfl_xor_sync(FULL, mloc[1], o));
+      }
+      float alpha[2], muse[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float mn = fmaxf(m_run[j], mloc[j]);
+        muse[j] = mn == -INFINITY ? 0.f : mn;
+        alpha[j] = ex2(m_run[j] - muse[j]);
+        m_run[j] = mn;
+      }
+      float pr[Cfg::kMTiles][4];
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[mt][e] = ex2(x[mt][e] - muse[e & 1]);
+      }
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        ls0 += pr[mt][0] + pr[mt][2];
+        ls1 += pr[mt][1] + pr[mt][3];
+      }
+      l_run[0] = l_run[0] * alpha[0] + ls0;
+      l_run[1] = l_run[1] * alpha[1] + ls1;
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) {
+        acc[dt][0] *= alpha[0];
+        acc[dt][1] *= alpha[1];
+        acc[dt][2] *= alpha[0];
+        acc[dt][3] *= alpha[1];
+      }
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        // Probabilities x 256 (exact) keep small ones out of f16 subnormals;
+        // the epilogue takes the factor back out.
+        const float q0 = pr[mt][0] * 256.f, q1 = pr[mt][1] * 256.f;
+        const float q2 = pr[mt][2] * 256.f, q3 = pr[mt][3] * 256.f;
+        const uint32_t hi0 = pack2<__half>(q0, q1);
+        const uint32_t hi1 = pack2<__half>(q2, q3);
+        const float2 f0 = unpack2<__half>(hi0), f1 = unpack2<__half>(hi1);
+        const uint32_t lo0 = pack2<__half>(q0 - f0.x, q1 - f0.y);
+        const uint32_t lo1 = pack2<__half>(q2 - f1.x, q3 - f1.y);
+        const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
+        const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
+        const int tok0 = 16 * mt + 4 * tig;
+        const uint8_t *va = vs + (tok0 / BS) * Cfg::kPageBytes + (tok0 % BS) + gid * BS;
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          const uint32_t wa = *reinterpret_cast<const uint32_t *>(va + (16 * dt) * BS);
+          const uint32_t wb = *reinterpret_cast<const uint32_t *>(va + (16 * dt + 8) * BS);
+          uint32_t a[4];
+          fp8x4_to_f16x2<KV>(wa, a[0], a[2]);
+          fp8x4_to_f16x2<KV>(wb, a[1], a[3]);
+          Mma16816<__half>::run(acc[dt], a, bh0, bh1);
+          Mma16816<__half>::run(acc[dt], a, bl0, bl1);
+        }
+      }
+      __syncwarp();
+      if (issued < my_n) issue_next();
+    }
+
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l_run[0] += __shfl_xor_sync(FULL, l_run[0], o);
+      l_run[1] += __shfl_xor_sync(FULL, l_run[1], o);
+    }
+    if (!ok) {
+      if (lane == 0) flag_error(p.err, 16u);
+      for (int i = waited; i < issued; ++i)
+        mbar_wait_bounded(&bars[i % NST], uint32_t(i / NST) & 1u,
+                          min(p.wait_limit_ns, uint64_t(100000000ull)));
+      __syncwarp();
+    }
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = 16 * dt + gid + 8 * (e >> 1);
+        const int h = 2 * tig + (e & 1);
+        epi[h * D + d] = acc[dt][e] * (1.f / 256.f);
+      }
+    }
+    if (lane < 4) {
+      epi[kMaxGroup * D + 2 * lane] = m_run[0];
+      epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
+      epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
+      epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
+    }
   } else {
     // ------------------------------------------------ fp32 CUDA-core body --
     constexpr int DL = D / 32;  // dims per lane: lane + 32*i
@@ -463,6 +705,10 @@ __global__ void __launch_bounds__(WARPS * 32)
         l_run[h] = 0.f;
       }
     }
+    float slh[kMaxGroup];  // ALiBi slopes, log2 units
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h)
+      slh[h] = (p.alibi != nullptr && h < g) ? p.alibi[h0 + h] * kLog2e : 0.f;
     for (int i = 0; i < my_n; ++i) {
       const int st = i % NST;
       const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u, p.wait_limit_ns);
@@ -473,6 +719,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       waited = i + 1;
       const int64_t c = warp + int64_t(WARPS) * i;
       const int nv = int(min(int64_t(CH), t1 - (t0 + c * CH)));
+      const int pb = int(t0 + c * CH) - L + 1;
       const float *kf = reinterpret_cast<const float *>(wbase + st * Cfg::kStageBytes);
       const float *vf = kf + CH * D;
       for (int tau = 0; tau < nv; ++tau) {
@@ -492,7 +739,8 @@ __global__ void __launch_bounds__(WARPS * 32)
             for (int i2 = 0; i2 < DL; ++i2) part = fmaf(qv[h][i2], kv[i2], part);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
-            const float xs = part * p.scale_log2;
+            float xs = part * p.scale_log2;
+            if (p.alibi != nullptr) xs = fmaf(slh[h], float(pb + tau), xs);
             const float mn = fmaxf(m_run[h], xs);
             const float a = ex2(m_run[h] - mn);
             const float pe = ex2(xs - mn);
@@ -549,7 +797,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       Ls = fmaf(f, ew[kMaxGroup * D + kMaxGroup + h], Ls);
       O = fmaf(f, ew[h * D + d], O);
     }
-    const float r = __fdiv_rn(O, Ls);
+    const float r = __fdiv_rn(O * p.out_scale, Ls);
     if (p.mode == kModeV1) {
       T *out = static_cast<T *>(p.out);
       out[int64_t(seq) * p.o_s0 + int64_t(h0 + h) * p.o_s1 + int64_t(d) * p.o_s2] = from_f32<T>(r);

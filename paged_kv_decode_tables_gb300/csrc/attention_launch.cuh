@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "../../include/paged_kv.h"
 #include "attention_kernel.cuh"
@@ -11,13 +12,11 @@
 
 namespace pkv {
 
-// Shared memory a (dtype, head_size, block_size, warps) instance needs, or 0
-// when that instance is not built.
-size_t attention_smem_bytes(pkv_dtype_t dtype, int head_size, int block_size, int warps);
-
-// Launch one instance on `grid` = (partitions, num_kv_heads, num_seqs).
-pkv_status_t launch_attention(pkv_dtype_t dtype, const AttnParams &p, int head_size,
-                              int block_size, int warps, dim3 grid, cudaStream_t stream);
+// Launch one instance on `grid` = (partitions, num_kv_heads * sub-groups,
+// num_seqs); `kv` selects the cache element format.
+pkv_status_t launch_attention(pkv_dtype_t dtype, pkv_kv_cache_dtype_t kv, const AttnParams &p,
+                              int head_size, int block_size, int warps, dim3 grid,
+                              cudaStream_t stream);
 
 namespace detail {
 
@@ -36,11 +35,11 @@ bool ensure_smem_attr(Kernel kernel, int bytes, std::atomic<unsigned long long> 
   return true;
 }
 
-template <typename T, int D, int BS, int W>
+template <typename T, typename KV, int D, int BS, int W>
 pkv_status_t launch_instance(const AttnParams &p, dim3 grid, cudaStream_t stream) {
-  using Cfg = AttnCfg<T, D, BS, W>;
+  using Cfg = AttnCfg<KV, D, BS, W>;
   static std::atomic<unsigned long long> done{0};
-  auto kernel = paged_attention_kernel<T, D, BS, W>;
+  auto kernel = paged_attention_kernel<T, KV, D, BS, W>;
   if (!ensure_smem_attr(kernel, Cfg::kSmemBytes, done)) return PKV_ERR_CUDA;
   return launch_programmatic(kernel, grid, dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) ==
                  cudaSuccess
@@ -50,63 +49,108 @@ pkv_status_t launch_instance(const AttnParams &p, dim3 grid, cudaStream_t stream
 
 // Instances are built for WARPS in {1, 2, 4}; a 4-warp instance only when its
 // shared memory stays within the per-CTA limit.
-template <typename T, int D, int BS, int W>
+template <typename KV, int D, int BS, int W>
 constexpr bool instance_fits() {
-  return AttnCfg<T, D, BS, W>::kSmemBytes <= 200 * 1024;
+  return AttnCfg<KV, D, BS, W>::kSmemBytes <= 200 * 1024;
 }
 
-template <typename T, int D, int BS>
+template <typename T, typename KV, int D, int BS>
 pkv_status_t launch_bs(const AttnParams &p, int warps, dim3 grid, cudaStream_t stream) {
-  if (warps == 1) return launch_instance<T, D, BS, 1>(p, grid, stream);
-  if constexpr (instance_fits<T, D, BS, 2>()) {
-    if (warps == 2) return launch_instance<T, D, BS, 2>(p, grid, stream);
+  if (warps == 1) return launch_instance<T, KV, D, BS, 1>(p, grid, stream);
+  if constexpr (instance_fits<KV, D, BS, 2>()) {
+    if (warps == 2) return launch_instance<T, KV, D, BS, 2>(p, grid, stream);
   }
-  if constexpr (instance_fits<T, D, BS, 4>()) {
-    if (warps == 4) return launch_instance<T, D, BS, 4>(p, grid, stream);
+  if constexpr (instance_fits<KV, D, BS, 4>()) {
+    if (warps == 4) return launch_instance<T, KV, D, BS, 4>(p, grid, stream);
   }
   return PKV_ERR_UNSUPPORTED;
 }
 
-template <typename T, int D, int BS>
+template <typename KV, int D, int BS>
 size_t smem_bs(int warps) {
-  if (warps == 1) return AttnCfg<T, D, BS, 1>::kSmemBytes;
-  if constexpr (instance_fits<T, D, BS, 2>()) {
-    if (warps == 2) return AttnCfg<T, D, BS, 2>::kSmemBytes;
+  if (warps == 1) return AttnCfg<KV, D, BS, 1>::kSmemBytes;
+  if constexpr (instance_fits<KV, D, BS, 2>()) {
+    if (warps == 2) return AttnCfg<KV, D, BS, 2>::kSmemBytes;
   }
-  if constexpr (instance_fits<T, D, BS, 4>()) {
-    if (warps == 4) return AttnCfg<T, D, BS, 4>::kSmemBytes;
+  if constexpr (instance_fits<KV, D, BS, 4>()) {
+    if (warps == 4) return AttnCfg<KV, D, BS, 4>::kSmemBytes;
   }
   return 0;
 }
 
-template <typename T, int D>
+template <typename T, typename KV, int D>
 pkv_status_t launch_d(const AttnParams &p, int BS, int W, dim3 g, cudaStream_t s) {
   switch (BS) {
-    case 8: return launch_bs<T, D, 8>(p, W, g, s);
-    case 16: return launch_bs<T, D, 16>(p, W, g, s);
-    case 32: return launch_bs<T, D, 32>(p, W, g, s);
+    case 8: return launch_bs<T, KV, D, 8>(p, W, g, s);
+    case 16: return launch_bs<T, KV, D, 16>(p, W, g, s);
+    case 32: return launch_bs<T, KV, D, 32>(p, W, g, s);
     default: return PKV_ERR_UNSUPPORTED;
   }
 }
 
-template <typename T, int D>
+template <typename KV, int D>
 size_t smem_d(int BS, int W) {
   switch (BS) {
-    case 8: return smem_bs<T, D, 8>(W);
-    case 16: return smem_bs<T, D, 16>(W);
-    case 32: return smem_bs<T, D, 32>(W);
+    case 8: return smem_bs<KV, D, 8>(W);
+    case 16: return smem_bs<KV, D, 16>(W);
+    case 32: return smem_bs<KV, D, 32>(W);
+    default: return 0;
+  }
+}
+
+// Head sizes built per element type: 64, 128, 256 (fp32: 64, 128).
+template <typename T>
+constexpr bool has_d256() {
+  return !std::is_same<T, float>::value;
+}
+
+template <typename T, typename KV>
+pkv_status_t launch_by_d(const AttnParams &p, int D, int BS, int W, dim3 g, cudaStream_t s) {
+  switch (D) {
+    case 64: return launch_d<T, KV, 64>(p, BS, W, g, s);
+    case 128: return launch_d<T, KV, 128>(p, BS, W, g, s);
+    case 256:
+      if constexpr (has_d256<T>()) return launch_d<T, KV, 256>(p, BS, W, g, s);
+      return PKV_ERR_UNSUPPORTED;
+    default: return PKV_ERR_UNSUPPORTED;
+  }
+}
+
+template <typename T, typename KV>
+size_t smem_by_d(int D, int BS, int W) {
+  switch (D) {
+    case 64: return smem_d<KV, 64>(BS, W);
+    case 128: return smem_d<KV, 128>(BS, W);
+    case 256:
+      if constexpr (has_d256<T>()) return smem_d<KV, 256>(BS, W);
+      return 0;
     default: return 0;
   }
 }
 
 }  // namespace detail
 
-// Per-dtype dispatch (one translation unit each).
-pkv_status_t launch_attention_f32(const AttnParams &p, int D, int BS, int W, dim3 g, cudaStream_t s);
-pkv_status_t launch_attention_f16(const AttnParams &p, int D, int BS, int W, dim3 g, cudaStream_t s);
-pkv_status_t launch_attention_bf16(const AttnParams &p, int D, int BS, int W, dim3 g, cudaStream_t s);
-size_t smem_attention_f32(int D, int BS, int W);
-size_t smem_attention_f16(int D, int BS, int W);
-size_t smem_attention_bf16(int D, int BS, int W);
+// Per (query dtype, cache format) dispatch, one translation unit each.
+#define PKV_DECLARE_ATTENTION(name)                                                      \
+  pkv_status_t launch_attention_##name(const AttnParams &p, int D, int BS, int W, dim3 g, \
+                                       cudaStream_t s);                                  \
+  size_t smem_attention_##name(int D, int BS, int W);
+PKV_DECLARE_ATTENTION(f32)
+PKV_DECLARE_ATTENTION(f16)
+PKV_DECLARE_ATTENTION(bf16)
+PKV_DECLARE_ATTENTION(f16_e4m3)
+PKV_DECLARE_ATTENTION(f16_e5m2)
+PKV_DECLARE_ATTENTION(bf16_e4m3)
+PKV_DECLARE_ATTENTION(bf16_e5m2)
+#undef PKV_DECLARE_ATTENTION
+
+#define PKV_DEFINE_ATTENTION(name, T, KV)                                                \
+  pkv_status_t launch_attention_##name(const AttnParams &p, int D, int BS, int W, dim3 g, \
+                                       cudaStream_t s) {                                 \
+    return detail::launch_by_d<T, KV>(p, D, BS, W, g, s);                                \
+  }                                                                                      \
+  size_t smem_attention_##name(int D, int BS, int W) {                                   \
+    return detail::smem_by_d<T, KV>(D, BS, W);                                           \
+  }
 
 }  // namespace pkv

@@ -208,6 +208,53 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
+// --------------------------------------------------------- fp8 cache codes --
+
+// Storage tags of one-byte KV-cache elements (OCP E4M3 / E5M2 codes).
+struct fp8_e4m3_t {
+  uint8_t bits;
+};
+struct fp8_e5m2_t {
+  uint8_t bits;
+};
+
+template <typename KV>
+struct is_fp8 {
+  static constexpr bool value = false;
+};
+template <>
+struct is_fp8<fp8_e4m3_t> {
+  static constexpr bool value = true;
+};
+template <>
+struct is_fp8<fp8_e5m2_t> {
+  static constexpr bool value = true;
+};
+
+// Four codes (bytes 0..3 of w) -> two f16x2 words: lo = {byte0, byte1},
+// hi = {byte2, byte3} (first byte in the low half).  Every E4M3 and E5M2 value
+// is exactly representable in f16.
+template <typename KV>
+__device__ __forceinline__ void fp8x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi);
+
+template <>
+__device__ __forceinline__ void fp8x4_to_f16x2<fp8_e4m3_t>(uint32_t w, uint32_t &lo,
+                                                          uint32_t &hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// An E5M2 code is the upper byte of the f16 with the same value (same
+// exponent width and bias), so widening is a byte move.
+template <>
+__device__ __forceinline__ void fp8x4_to_f16x2<fp8_e5m2_t>(uint32_t w, uint32_t &lo,
+                                                          uint32_t &hi) {
+  lo = __byte_perm(w, 0u, 0x1404u);
+  hi = __byte_perm(w, 0u, 0x3424u);
+}
+
 __device__ __forceinline__ void flag_error(int32_t *err, uint32_t bit) {
   if (err) atomicOr(reinterpret_cast<unsigned int *>(err), bit);
 }

@@ -48,12 +48,26 @@ def assert_attention_close(got: torch.Tensor, ref: torch.Tensor, dtype: torch.dt
     return float(diff[mask].max()) if bool(mask.any()) else 0.0
 
 
+def variant_kwargs(g):
+    """Cache format and ALiBi arguments of an input dict (defaults: plain)."""
+    return dict(kv_cache_dtype=g.get("kv_cache_dtype", "auto"), k_scale=g.get("k_scale", 1.0),
+                v_scale=g.get("v_scale", 1.0), alibi_slopes=g.get("alibi_slopes"))
+
+
+def oracle_kwargs(inp):
+    """The same arguments for the oracle (slopes as a host list)."""
+    kw = variant_kwargs(inp)
+    if kw["alibi_slopes"] is not None:
+        kw["alibi_slopes"] = [float(v) for v in kw["alibi_slopes"].cpu()]
+    return kw
+
+
 def run_v1(g, *, err=None, block_tables=None, kv_indptr=None, stream=None):
     out = torch.empty_like(g["query"])
     pkv.paged_attention_decode(out, g["query"], g["key_cache"], g["value_cache"],
                                g["block_tables"] if block_tables is None else block_tables,
                                g["seq_lens"], g["scale"], kv_indptr=kv_indptr, err_flag=err,
-                               stream=stream)
+                               stream=stream, **variant_kwargs(g))
     return out
 
 
@@ -67,7 +81,8 @@ def run_v2(g, max_parts, *, partition_size=512, splits=None, err=None, block_tab
     pkv.paged_attention_v2_partition(tmp, es, ml, g["query"], g["key_cache"], g["value_cache"],
                                      g["block_tables"] if block_tables is None else block_tables,
                                      g["seq_lens"], g["scale"], partition_size=partition_size,
-                                     num_kv_splits=splits, kv_indptr=kv_indptr, err_flag=err)
+                                     num_kv_splits=splits, kv_indptr=kv_indptr, err_flag=err,
+                                     **variant_kwargs(g))
     out = torch.empty_like(g["query"])
     pkv.paged_attention_v2_reduce(out, tmp, es, ml, g["seq_lens"], partition_size=partition_size,
                                   num_kv_splits=splits, block_size=g["block_size"], err_flag=err)

@@ -120,6 +120,32 @@ def test_decode_rejects_noncontiguous_pages_and_misalignment(lib):
     assert _decode(lib, _args(), out=0) == 1
 
 
+def _fp8_args(**kw):
+    """Valid arguments for a bf16-query decode over an fp8 cache (x = 16)."""
+    a = _args(kv_cache_dtype=1, k_scale=0.5, v_scale=2.0, x=16)
+    a.k_stride[:] = [2 * 8 * 16 * 16, 8 * 16 * 16, 16 * 16, 16, 1]
+    a.v_stride[:] = [2 * 128 * 16, 128 * 16, 16, 1]
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_fp8_cache_and_alibi_argument_checks(lib):
+    assert _decode(lib, _fp8_args(num_seqs=0)) == 0        # valid, nothing to do
+    assert _decode(lib, _fp8_args(kv_cache_dtype=3)) == 1   # unknown cache format
+    assert _decode(lib, _fp8_args(dtype=0)) == 2            # fp32 queries over fp8: not built
+    assert _decode(lib, _fp8_args(k_scale=float("inf"))) == 1
+    assert _decode(lib, _fp8_args(v_scale=float("nan"))) == 1
+    assert _decode(lib, _fp8_args(x=8)) == 1                # x * 1 byte != 16
+    a = _fp8_args()
+    a.k_stride[0] += 8                                      # 8-byte block stride
+    assert _decode(lib, a) == 1
+    assert _decode(lib, _args(alibi_slopes=0x2002)) == 1    # slopes not 4-byte aligned
+    assert _decode(lib, _args(num_seqs=0, alibi_slopes=0x2004)) == 0
+    # auto caches ignore the scales, even non-finite ones
+    assert _decode(lib, _args(num_seqs=0, k_scale=float("nan"))) == 0
+
+
 def test_empty_batch_is_a_no_op(lib):
     assert _decode(lib, _args(num_seqs=0)) == 0
     assert lib.copy_page_indices(0, 0, 0, 0, 0, 0, 0, 0, None, None) == 0

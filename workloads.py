@@ -48,6 +48,18 @@ def x_pack(dtype: torch.dtype) -> int:
     return 16 // torch.empty((), dtype=dtype).element_size()
 
 
+# kv_cache_dtype names -> torch float8 type used to round the drawn values
+FP8_TORCH = {"fp8": torch.float8_e4m3fn, "fp8_e4m3": torch.float8_e4m3fn,
+             "fp8_e5m2": torch.float8_e5m2}
+
+
+def alibi_slopes(num_heads: int) -> torch.Tensor:
+    """Per-head ALiBi slopes 2^(-8 (h+1) / num_heads): the geometric sequence of
+    "Train Short, Test Long" (Press et al.), used here only as an input."""
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / num_heads) for h in range(num_heads)],
+                        dtype=torch.float32)
+
+
 @dataclass
 class WorkloadSpec:
     """Shape and value recipe of one synthetic decode batch."""
@@ -163,6 +175,10 @@ def make_inputs(
     unused_slot_fill: Optional[float] = None,
     seed: int = 0,
     device="cpu",
+    kv_cache_dtype: str = "auto",
+    k_scale: float = 1.0,
+    v_scale: float = 1.0,
+    alibi: bool = False,
 ) -> Dict:
     """Draw one paged decode batch.
 
@@ -182,12 +198,22 @@ def make_inputs(
       and returned as the column view ``[:, ::bt_col_step]``; entries that no
       sequence owns hold -1, skipped columns hold -7.
 
+    * ``kv_cache_dtype`` "fp8" / "fp8_e4m3" / "fp8_e5m2": the caches hold one-byte
+      codes (uint8 tensors, ``x = 16``): the same float32 draws rounded once to
+      that float8 format; ``k_scale`` / ``v_scale`` are returned for the
+      consumer (the codes do not depend on them).
+    * ``alibi``: also return ``alibi_slopes`` (float32 ``[num_heads]``).
+
     Random draws happen on ``device`` (a CUDA generator when it is a GPU) so
     multi-GB batches need no host-side generation; small batches default to
     the CPU.  Returned tensors live on ``device``.
     """
     dt = DTYPES[dtype]
-    x = x_pack(dt)
+    fp8 = FP8_TORCH.get(kv_cache_dtype)
+    if kv_cache_dtype != "auto" and fp8 is None:
+        raise ValueError(f"unknown kv_cache_dtype {kv_cache_dtype!r}")
+    cache_dt = torch.uint8 if fp8 is not None else dt
+    x = 16 if fp8 is not None else x_pack(dt)
     seq_lens = [int(v) for v in seq_lens]
     B = len(seq_lens)
     if head_size % x:
@@ -236,8 +262,12 @@ def make_inputs(
     g_k = _gen(seed, 4, device)
     g_v = _gen(seed, 5, device)
     query = torch.randn((B, num_heads, D), generator=g_q, device=device, dtype=torch.float32).to(dt)
-    key_cache = torch.empty((num_blocks, Hk, D // x, block_size, x), dtype=dt, device=device)
-    value_cache = torch.empty((num_blocks, Hk, D, block_size), dtype=dt, device=device)
+    key_cache = torch.empty((num_blocks, Hk, D // x, block_size, x), dtype=cache_dt, device=device)
+    value_cache = torch.empty((num_blocks, Hk, D, block_size), dtype=cache_dt, device=device)
+
+    def rounded(v):
+        return v.to(dt) if fp8 is None else v.to(fp8).view(torch.uint8)
+
     # Draw block by block in slabs to bound float32 temporaries.
     slab = max(1, (1 << 26) // (Hk * D * block_size))
     g_p = _gen(seed, 6, device)
@@ -249,10 +279,10 @@ def make_inputs(
             u = torch.rand((b1 - b0, Hk, 1, block_size, 1), generator=g_p, device=device,
                            dtype=torch.float32)
             kk = torch.where(u < peaky_fraction, kk * peaky_scale, kk)
-        key_cache[b0:b1] = kk.to(dt)
+        key_cache[b0:b1] = rounded(kk)
         vv = torch.randn((b1 - b0, Hk, D, block_size), generator=g_v, device=device,
                          dtype=torch.float32)
-        value_cache[b0:b1] = vv.to(dt)
+        value_cache[b0:b1] = rounded(vv)
         del kk, vv
 
     if unused_slot_fill is not None:
@@ -264,8 +294,12 @@ def make_inputs(
         owned = owned.to(device)
         kmask = (~owned).view(num_blocks, 1, 1, block_size, 1).expand_as(key_cache)
         vmask = (~owned).view(num_blocks, 1, 1, block_size).expand_as(value_cache)
-        key_cache[kmask] = unused_slot_fill
-        value_cache[vmask] = unused_slot_fill
+        fill = unused_slot_fill
+        if fp8 is not None:
+            fill = int(torch.tensor([unused_slot_fill], dtype=torch.float32).to(fp8)
+                       .view(torch.uint8)[0])
+        key_cache[kmask] = fill
+        value_cache[vmask] = fill
 
     seq_lens_t = torch.tensor(seq_lens, dtype=torch.int32, device=device)
     return {
@@ -286,6 +320,10 @@ def make_inputs(
         "dtype": dtype,
         "scale": 1.0 / math.sqrt(D),
         "max_blocks_per_seq": max_blocks_per_seq,
+        "kv_cache_dtype": kv_cache_dtype,
+        "k_scale": float(k_scale),
+        "v_scale": float(v_scale),
+        "alibi_slopes": alibi_slopes(num_heads).to(device) if alibi else None,
     }
 
 
