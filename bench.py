@@ -186,8 +186,9 @@ class DecodeStep:
         lens = inp["seq_lens_list"]
         self.lens = lens
         e = q.element_size()
+        ekv = kc.element_size()  # 1 for an fp8 cache
         nblk = [len(r) for r in inp["block_rows"]]
-        self.kv_bytes = sum(lens) * Hk * 2 * D * e
+        self.kv_bytes = sum(lens) * Hk * 2 * D * ekv
         self.q_bytes = B * H * D * e
         self.out_bytes = B * H * D * e
         self.table_bytes = 4 * sum(nblk)
@@ -217,7 +218,8 @@ class DecodeStep:
             self.ml = torch.empty(B, H, self.maxP, dtype=torch.float32, device=dev)
             self.partial_bytes = 0
         self.args = pkv._decode_args(q, kc, vc, bt_for_attn, inp["seq_lens"], inp["scale"], indptr,
-                                     None, None)
+                                     None, None, spec.kv_cache_dtype, spec.k_scale, spec.v_scale,
+                                     inp["alibi_slopes"])
         self.args_ref = ctypes.byref(self.args)
         self.fused_metadata = fused_metadata
         self.launches_per_step = {"v1": 1, "v2_fixed": 2,
@@ -227,7 +229,8 @@ class DecodeStep:
         # pass) its output.  The fp32 split-KV partials are counted apart.
         self.attn_alg_bytes = (self.kv_bytes + self.q_bytes + self.table_bytes + 4 * B +
                                (self.out_bytes if self.mode == "v1" else 0) +
-                               (4 * B + 4 * (B + 1) if self.mode == "v2_splits" else 0))
+                               (4 * B + 4 * (B + 1) if self.mode == "v2_splits" else 0) +
+                               (4 * H if spec.alibi else 0))
 
     def _check(self, st, what):
         if st != 0:
@@ -370,22 +373,31 @@ def oracle_step(inp, spec, seq_ids, all_splits):
     import oracle
 
     q, kc, vc, bt, lens = oracle_sample_inputs(inp, seq_ids)
+    kw = oracle_variant_kwargs(inp)
     t0 = time.perf_counter()
     if spec.mode == "v1":
-        oracle.decode_v1(q, kc, vc, bt, lens, inp["scale"])
+        oracle.decode_v1(q, kc, vc, bt, lens, inp["scale"], **kw)
     elif spec.mode == "v2_fixed":
         maxP = -(-max(lens) // spec.partition_size)
         tmp, es, ml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], maxP,
-                                          partition_size=spec.partition_size)
+                                          partition_size=spec.partition_size, **kw)
         oracle.v2_reduce(tmp, es, ml, lens, spec.block_size, partition_size=spec.partition_size)
     else:
         splits = [all_splits[s] for s in seq_ids]
         tmp, es, ml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], spec.max_kv_splits,
-                                          num_kv_splits=splits)
+                                          num_kv_splits=splits, **kw)
         oracle.v2_reduce(tmp, es, ml, lens, spec.block_size, num_kv_splits=splits)
     dt = time.perf_counter() - t0
-    e = inp["query"].element_size()
+    e = inp["key_cache"].element_size()
     return sum(lens) * spec.num_kv_heads * 2 * spec.head_size * e, dt
+
+
+def oracle_variant_kwargs(inp):
+    """Cache format and ALiBi slopes of a workload, as the oracle takes them."""
+    sl = inp.get("alibi_slopes")
+    return dict(kv_cache_dtype=inp.get("kv_cache_dtype", "auto"), k_scale=inp.get("k_scale", 1.0),
+                v_scale=inp.get("v_scale", 1.0),
+                alibi_slopes=None if sl is None else [float(v) for v in sl.cpu()])
 
 
 def cpu_threads():
@@ -649,7 +661,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if spec.dtype == "bf16" else spec.dtype,
+        "dtype": spec.dtype if spec.kv_cache_dtype == "auto" else f"{spec.dtype}+{spec.kv_cache_dtype}",
         "accumulate": "f32",
         "data": "synthetic (seeded; see workloads.py)",
         "config": {
@@ -657,6 +669,7 @@ def run_ours(args):
             "description": spec.description,
             "num_seqs": step.B, "num_heads": step.H, "num_kv_heads": step.Hk,
             "head_size": step.D, "block_size": step.bs,
+            "kv_cache_dtype": spec.kv_cache_dtype, "alibi": spec.alibi,
             "total_tokens": sum(step.lens), "kv_bytes_per_step": step.kv_bytes,
             "l2": ("flushed between steps (512 MB write)" if flush else
                    f"inputs larger than L2: {step.kv_bytes / 1e9:.2f} GB of K/V per step"),

@@ -97,7 +97,11 @@ template <typename KV, int D, int BS, int WARPS>
 struct AttnCfg {
   static constexpr int kElem = int(sizeof(KV));
   static constexpr int kX = 16 / kElem;
-  static constexpr int kChunk = BS >= 16 ? BS : 16;  // tokens per pipeline stage
+  // Tokens per pipeline stage: at least 16 (one MMA tile), 32 for one-byte
+  // caches so that a stage's serial softmax step covers as many bytes as a
+  // 16-bit cache's.
+  static constexpr int kMinChunk = kElem == 1 ? 32 : 16;
+  static constexpr int kChunk = BS >= kMinChunk ? BS : kMinChunk;
   static constexpr int kPagesPerChunk = kChunk / BS;
   static constexpr int kMTiles = kChunk / 16;
   static constexpr int kPageBytes = D * BS * kElem;    // one K (or V) page
@@ -420,12 +424,16 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
       l_run[0] = l_run[0] * alpha[0] + ls0;
       l_run[1] = l_run[1] * alpha[1] + ls1;
+      // alpha is exactly 1 wherever the running max did not grow; once it
+      // settles, whole chunks skip the rescale (x 1 would change nothing).
+      if (__any_sync(FULL, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-      for (int dt = 0; dt < DT; ++dt) {
-        acc[dt][0] *= alpha[0];
-        acc[dt][1] *= alpha[1];
-        acc[dt][2] *= alpha[0];
-        acc[dt][3] *= alpha[1];
+        for (int dt = 0; dt < DT; ++dt) {
+          acc[dt][0] *= alpha[0];
+          acc[dt][1] *= alpha[1];
+          acc[dt][2] *= alpha[0];
+          acc[dt][3] *= alpha[1];
+        }
       }
 #pragma unroll
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
@@ -566,20 +574,27 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        const int ta = 16 * mt + rA, tb = ta + 2;
-        const uint8_t *ka = ks + (ta / BS) * Cfg::kPageBytes + (ta % BS) * 16 + 4 * tig;
-        const uint8_t *kb = ks + (tb / BS) * Cfg::kPageBytes + (tb % BS) * 16 + 4 * tig;
+        // One ldmatrix.x4 returns, per lane, the code words (bytes 4tig..4tig+3
+        // of a 16-byte key row) of rows gid (token rA) and gid+8 (token rA+2)
+        // for two 16-dim groups: lane l addresses row l%8 of matrix l/8, i.e.
+        // token rA(l%8) + 2*((l/8)&1) of group k2 + l/16.
+        const int lt = 16 * mt + 4 * ((lane & 7) >> 1) + (lane & 1) + 2 * ((lane >> 3) & 1);
+        const uint32_t krow = smem_addr(ks) + (lt / BS) * Cfg::kPageBytes +
+                              ((lane >> 4) * BS + (lt % BS)) * 16;
 #pragma unroll
-        for (int k2 = 0; k2 < DT; ++k2) {
-          const uint32_t wa = *reinterpret_cast<const uint32_t *>(ka + k2 * (BS * 16));
-          const uint32_t wb = *reinterpret_cast<const uint32_t *>(kb + k2 * (BS * 16));
-          uint32_t a[4];
-          fp8x4_to_f16x2<KV>(wa, a[0], a[2]);
-          fp8x4_to_f16x2<KV>(wb, a[1], a[3]);
-          if (k2 & 1)
-            Mma16816<__half>::run(s1, a, qf[k2][0], qf[k2][1]);
-          else
-            Mma16816<__half>::run(s0, a, qf[k2][0], qf[k2][1]);
+        for (int k2 = 0; k2 < DT; k2 += 2) {
+          uint32_t w[4];
+          ldsm_x4(krow + k2 * (BS * 16), w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t a[4];
+            fp8x4_to_f16x2<KV>(w[2 * h], a[0], a[2]);
+            fp8x4_to_f16x2<KV>(w[2 * h + 1], a[1], a[3]);
+            if (h)
+              Mma16816<__half>::run(s1, a, qf[k2 + h][0], qf[k2 + h][1]);
+            else
+              Mma16816<__half>::run(s0, a, qf[k2 + h][0], qf[k2 + h][1]);
+          }
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -622,12 +637,16 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
       l_run[0] = l_run[0] * alpha[0] + ls0;
       l_run[1] = l_run[1] * alpha[1] + ls1;
+      // alpha is exactly 1 wherever the running max did not grow; once it
+      // settles, whole chunks skip the rescale (x 1 would change nothing).
+      if (__any_sync(FULL, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-      for (int dt = 0; dt < DT; ++dt) {
-        acc[dt][0] *= alpha[0];
-        acc[dt][1] *= alpha[1];
-        acc[dt][2] *= alpha[0];
-        acc[dt][3] *= alpha[1];
+        for (int dt = 0; dt < DT; ++dt) {
+          acc[dt][0] *= alpha[0];
+          acc[dt][1] *= alpha[1];
+          acc[dt][2] *= alpha[0];
+          acc[dt][3] *= alpha[1];
+        }
       }
 #pragma unroll
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
@@ -642,17 +661,40 @@ __global__ void __launch_bounds__(WARPS * 32)
         const uint32_t lo1 = pack2<__half>(q2 - f1.x, q3 - f1.y);
         const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
         const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
-        const int tok0 = 16 * mt + 4 * tig;
-        const uint8_t *va = vs + (tok0 / BS) * Cfg::kPageBytes + (tok0 % BS) + gid * BS;
+        if constexpr (BS >= 16) {
+          // A value row holds a dim's 16 tokens of the tile in 16 bytes: one
+          // ldmatrix.x4 gives the words of dims gid, gid+8 for two dim tiles
+          // (lane l addresses dim 16*(l/16) + 8*((l/8)&1) + l%8).
+          const int ld = 16 * (lane >> 4) + 8 * ((lane >> 3) & 1) + (lane & 7);
+          const uint32_t vrow = smem_addr(vs) + ((16 * mt) / BS) * Cfg::kPageBytes +
+                                (16 * mt) % BS + ld * BS;
 #pragma unroll
-        for (int dt = 0; dt < DT; ++dt) {
-          const uint32_t wa = *reinterpret_cast<const uint32_t *>(va + (16 * dt) * BS);
-          const uint32_t wb = *reinterpret_cast<const uint32_t *>(va + (16 * dt + 8) * BS);
-          uint32_t a[4];
-          fp8x4_to_f16x2<KV>(wa, a[0], a[2]);
-          fp8x4_to_f16x2<KV>(wb, a[1], a[3]);
-          Mma16816<__half>::run(acc[dt], a, bh0, bh1);
-          Mma16816<__half>::run(acc[dt], a, bl0, bl1);
+          for (int dt = 0; dt < DT; dt += 2) {
+            uint32_t w[4];
+            ldsm_x4(vrow + (16 * dt) * BS, w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t a[4];
+              fp8x4_to_f16x2<KV>(w[2 * h], a[0], a[2]);
+              fp8x4_to_f16x2<KV>(w[2 * h + 1], a[1], a[3]);
+              Mma16816<__half>::run(acc[dt + h], a, bh0, bh1);
+              Mma16816<__half>::run(acc[dt + h], a, bl0, bl1);
+            }
+          }
+        } else {
+          // 8-token pages: the tile's 16 tokens of a dim sit in two pages.
+          const int tok0 = 16 * mt + 4 * tig;
+          const uint8_t *va = vs + (tok0 / BS) * Cfg::kPageBytes + (tok0 % BS) + gid * BS;
+#pragma unroll
+          for (int dt = 0; dt < DT; ++dt) {
+            const uint32_t wa = *reinterpret_cast<const uint32_t *>(va + (16 * dt) * BS);
+            const uint32_t wb = *reinterpret_cast<const uint32_t *>(va + (16 * dt + 8) * BS);
+            uint32_t a[4];
+            fp8x4_to_f16x2<KV>(wa, a[0], a[2]);
+            fp8x4_to_f16x2<KV>(wb, a[1], a[3]);
+            Mma16816<__half>::run(acc[dt], a, bh0, bh1);
+            Mma16816<__half>::run(acc[dt], a, bl0, bl1);
+          }
         }
       }
       __syncwarp();

@@ -11,6 +11,7 @@ import torch
 
 import bench
 import oracle
+import workloads
 from gpu_support import assert_attention_close, assert_partials_close
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -43,15 +44,25 @@ def _run_step(name):
     return step
 
 
+def _value_range(inp):
+    """Largest |value| the cache stands for (fp8: decoded code x v_scale)."""
+    vc = inp["value_cache"]
+    if inp["kv_cache_dtype"] != "auto":
+        return float(vc.view(workloads.FP8_TORCH[inp["kv_cache_dtype"]]).float().abs().max()) * \
+            inp["v_scale"]
+    return float(vc.float().abs().max())
+
+
 @pytest.mark.parametrize("name", ["mha_v1_fp16", "gqa_v1_bf16", "long_v2_bf16", "ragged_v2_bf16",
-                                  "tiny_mha_fp32"])
+                                  "tiny_mha_fp32", "ragged_v2_fp8", "long_v2_fp8",
+                                  "mha_v1_alibi_fp16"])
 def test_full_size_workload(name):
     step = _run_step(name)
     inp, spec = step.inp, step.spec
     out = step.out
     assert bool(torch.isfinite(out).all()), "non-finite output"
-    vmax = float(inp["value_cache"].float().abs().max())
-    assert float(out.float().abs().max()) <= vmax + 1e-3
+    vmax = _value_range(inp)
+    assert float(out.float().abs().max()) <= vmax * (1 + 2 ** -7) + 1e-3
 
     splits = None
     if spec.mode == "v2_splits":
@@ -65,7 +76,8 @@ def test_full_size_workload(name):
 
     seqs = _samples(step.lens)
     q, kc, vc, bt, lens = bench.oracle_sample_inputs(inp, seqs)
-    ref = oracle.decode_v1(q, kc, vc, bt, lens, inp["scale"])
+    kw = bench.oracle_variant_kwargs(inp)
+    ref = oracle.decode_v1(q, kc, vc, bt, lens, inp["scale"], **kw)
     got = out[torch.tensor(seqs, device=out.device)]
     assert_attention_close(got, ref, DT[spec.dtype], f"{name} sampled outputs")
 
@@ -74,10 +86,10 @@ def test_full_size_workload(name):
         if spec.mode == "v2_fixed":
             maxP = step.maxP
             rtmp, res, rml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], maxP,
-                                                 partition_size=spec.partition_size)
+                                                 partition_size=spec.partition_size, **kw)
         else:
             maxP = step.maxP
             rtmp, res, rml = oracle.v2_partition(q, kc, vc, bt, lens, inp["scale"], maxP,
-                                                 num_kv_splits=[splits[s] for s in seqs])
+                                                 num_kv_splits=[splits[s] for s in seqs], **kw)
         assert_partials_close(step.tmp[sel], step.es[sel], step.ml[sel], rtmp, res, rml,
                               f"{name} sampled partials")

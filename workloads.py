@@ -15,8 +15,8 @@ Cache layouts are the vLLM ones restated on the page "paged_attention_v2_triton.
 * ``block_tables`` ``[num_seqs, max_blocks_per_seq]`` int32 (may be a strided view)
 * ``seq_lens``     ``[num_seqs]`` int32
 
-Named workloads (``WORKLOADS``) reproduce the five decode batches this library
-is measured on; each is described by what it is and its sizes.
+Named workloads (``WORKLOADS``) are the decode batches this library is
+measured on; each is described by what it is and its sizes.
 """
 from __future__ import annotations
 
@@ -88,6 +88,10 @@ class WorkloadSpec:
     partition_size: int = 512
     max_kv_splits: int = 16
     device_core_count: int = 148
+    kv_cache_dtype: str = "auto"  # or "fp8_e4m3" / "fp8_e5m2": one-byte cache codes
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+    alibi: bool = False
     extra: Dict = field(default_factory=dict)
 
 
@@ -133,6 +137,38 @@ WORKLOADS: Dict[str, WorkloadSpec] = {
         seq_len_recipe="lognormal", lognormal_median=1024.0, lognormal_sigma=1.0,
         seq_len_lo=1, seq_len_hi=32768, bt_col_step=2, max_blocks_per_seq=2048,
         mode="v2_splits", max_kv_splits=16, device_core_count=148,
+    ),
+    "ragged_v2_fp8": WorkloadSpec(
+        name="ragged_v2_fp8",
+        description=("ragged serving batch + metadata over an fp8 E4M3 cache: the ragged bf16 "
+                     "batch (512 seqs, log-normal seq_lens, 32 query heads / 8 kv heads, head_size "
+                     "128, block_size 16, stride-2 table view, split-KV) with one-byte key/value "
+                     "codes, bf16 queries and output, k_scale 0.5, v_scale 2"),
+        num_seqs=512, num_heads=32, num_kv_heads=8, head_size=128, block_size=16, dtype="bf16",
+        seq_len_recipe="lognormal", lognormal_median=1024.0, lognormal_sigma=1.0,
+        seq_len_lo=1, seq_len_hi=32768, bt_col_step=2, max_blocks_per_seq=2048,
+        mode="v2_splits", max_kv_splits=16, device_core_count=148,
+        kv_cache_dtype="fp8_e4m3", k_scale=0.5, v_scale=2.0,
+    ),
+    "long_v2_fp8": WorkloadSpec(
+        name="long_v2_fp8",
+        description=("long-context split-KV decode over an fp8 E4M3 cache: 8 seqs of 16k..128k "
+                     "tokens, 64 query heads / 8 kv heads, head_size 128, block_size 16, "
+                     "partition 512, 1% of keys x8, bf16 queries and output, k_scale 0.5, "
+                     "v_scale 2"),
+        num_seqs=8, num_heads=64, num_kv_heads=8, head_size=128, block_size=16, dtype="bf16",
+        seq_len_recipe="fixed",
+        seq_lens=[k * 1024 for k in (16, 24, 32, 48, 64, 96, 112, 128)],
+        peaky_fraction=0.01, peaky_scale=8.0, mode="v2_fixed", partition_size=512,
+        kv_cache_dtype="fp8_e4m3", k_scale=0.5, v_scale=2.0,
+    ),
+    "mha_v1_alibi_fp16": WorkloadSpec(
+        name="mha_v1_alibi_fp16",
+        description=("MHA single-pass decode with ALiBi, fp16: the MHA batch (64 seqs, 32 heads = "
+                     "32 kv heads, head_size 128, block_size 16, seq_lens uniform in [512, 4096]) "
+                     "with slopes 2^(-8(h+1)/32)"),
+        num_seqs=64, num_heads=32, num_kv_heads=32, head_size=128, block_size=16, dtype="f16",
+        seq_len_recipe="uniform", seq_len_lo=512, seq_len_hi=4096, mode="v1", alibi=True,
     ),
 }
 
@@ -348,6 +384,10 @@ def make_workload(name: str, seed: int = 0, device="cpu", **overrides) -> Dict:
         peaky_scale=spec.peaky_scale,
         seed=seed,
         device=device,
+        kv_cache_dtype=spec.kv_cache_dtype,
+        k_scale=spec.k_scale,
+        v_scale=spec.v_scale,
+        alibi=spec.alibi,
     )
     # cu_num_blocks: the indptr a serving engine hands to the page-index copy
     # (exclusive scan of each sequence's block count).
