@@ -97,18 +97,21 @@ template <typename KV, int D, int BS, int WARPS>
 struct AttnCfg {
   static constexpr int kElem = int(sizeof(KV));
   static constexpr int kX = 16 / kElem;
-  // Tokens per pipeline stage: at least 16 (one MMA tile), 32 for one-byte
-  // caches so that a stage's serial softmax step covers as many bytes as a
-  // 16-bit cache's.
-  static constexpr int kMinChunk = kElem == 1 ? 32 : 16;
+  // Tokens per pipeline stage: at least 16 (one MMA tile); 32 for one-byte
+  // caches up to head size 128, so that a stage's serial softmax step covers
+  // as many bytes as a 16-bit cache's (at head size 256 a 16-token stage
+  // already holds 8 KiB, and longer ones cost resident warps).
+  static constexpr int kMinChunk = (kElem == 1 && D <= 128) ? 32 : 16;
   static constexpr int kChunk = BS >= kMinChunk ? BS : kMinChunk;
   static constexpr int kPagesPerChunk = kChunk / BS;
   static constexpr int kMTiles = kChunk / 16;
   static constexpr int kPageBytes = D * BS * kElem;    // one K (or V) page
   static constexpr int kHalfStage = kChunk * D * kElem;  // K (or V) part of a stage
   static constexpr int kStageBytes = 2 * kHalfStage;
-  static constexpr int kWarpBudget = 16 * 1024;
-  static constexpr int kStages = clamp_int(kWarpBudget / kStageBytes, 2, 8);
+  // Two stages per warp: measured, more resident warps beat deeper per-warp
+  // rings at every head size (a 16 KiB ring of 4 KiB stages at head size 64
+  // loses 2-25 % to two stages).
+  static constexpr int kStages = 2;
   static constexpr int kWarpBytes = kStages * kStageBytes;
   static constexpr int kEpiFloats = kMaxGroup * D + 2 * kMaxGroup;
   static constexpr int kSmemBytes = WARPS * kWarpBytes + WARPS * kStages * 8;
