@@ -97,11 +97,12 @@ template <typename KV, int D, int BS, int WARPS>
 struct AttnCfg {
   static constexpr int kElem = int(sizeof(KV));
   static constexpr int kX = 16 / kElem;
-  // Tokens per pipeline stage: at least 16 (one MMA tile); 32 for one-byte
-  // caches up to head size 128, so that a stage's serial softmax step covers
-  // as many bytes as a 16-bit cache's (at head size 256 a 16-token stage
-  // already holds 8 KiB, and longer ones cost resident warps).
-  static constexpr int kMinChunk = (kElem == 1 && D <= 128) ? 32 : 16;
+  // Tokens per pipeline stage: at least 16 (one MMA tile).  One-byte caches
+  // with one warp per CTA take 32 up to head size 128, so that a stage's
+  // serial softmax step covers as many bytes as a 16-bit cache's; with more
+  // warps per CTA the smaller ring keeps more warps resident, which measured
+  // faster (at head size 256 a 16-token stage already holds 8 KiB).
+  static constexpr int kMinChunk = (kElem == 1 && D <= 128 && WARPS == 1) ? 32 : 16;
   static constexpr int kChunk = BS >= kMinChunk ? BS : kMinChunk;
   static constexpr int kPagesPerChunk = kChunk / BS;
   static constexpr int kMTiles = kChunk / 16;
