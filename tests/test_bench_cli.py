@@ -32,3 +32,23 @@ def test_reference_arm_declines_library_only_workloads():
     assert out.returncode == 0
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and "unavailable" in line
+
+
+def test_oracle_step_covers_fp8_and_alibi_workloads():
+    """The CPU leg runs the oracle with the workload's cache format and
+    slopes, and counts one byte per fp8 cache element."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    for name in ("ragged_v2_fp8", "mha_v1_alibi_fp16"):
+        inp = workloads.make_workload(name, seed=0, num_seqs=3)
+        spec = inp["spec"]
+        kw = bench.oracle_variant_kwargs(inp)
+        assert kw["kv_cache_dtype"] == spec.kv_cache_dtype
+        assert (kw["alibi_slopes"] is not None) == spec.alibi
+        splits = bench.oracle_metadata(inp, spec)
+        nbytes, seconds = bench.oracle_step(inp, spec, [0, 2], splits)
+        e = 1 if spec.kv_cache_dtype != "auto" else 2
+        lens = inp["seq_lens_list"]
+        assert nbytes == (lens[0] + lens[2]) * spec.num_kv_heads * 2 * spec.head_size * e
+        assert seconds > 0
