@@ -122,8 +122,18 @@ struct AttnCfg {
   static_assert(kHalfStage % 16 == 0 && kPageBytes % 16 == 0, "bulk copies need 16 B");
 };
 
+// CTAs per SM an instance is compiled to keep resident (0: no floor).
+// Measured for fp8 caches with two warps per CTA up to head size 128: a floor
+// of 10 CTAs (96 registers, a few bytes of spill) beats the 8 that 127
+// registers allow (ragged batch 360 -> 347 us); 9 CTAs gain nothing, and one
+// or four warps per CTA lose.
+template <typename KV, int D, int WARPS>
+constexpr int resident_ctas() {
+  return (is_fp8<KV>::value && D <= 128 && WARPS == 2) ? 10 : 0;
+}
+
 template <typename T, typename KV, int D, int BS, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     paged_attention_kernel(const AttnParams p) {
   using Cfg = AttnCfg<KV, D, BS, WARPS>;
   constexpr bool kFp8 = is_fp8<KV>::value;
