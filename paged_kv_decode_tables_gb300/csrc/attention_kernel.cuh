@@ -1,18 +1,20 @@
 // Paged decode attention kernel: single-pass (v1) and split-KV partition (v2).
 //
-// One CTA per (partition, kv_head, sequence).  The CTA serves every query
-// head of the kv head's GQA group at once, so each K/V byte crosses HBM once
-// (page "paged_attention_v2_triton.py": per instance, load Q, gather K/V of the
+// One CTA per (partition, kv_head x query-head sub-group, sequence).  The CTA
+// serves up to 8 query heads of the kv head's GQA group at once (all of them
+// for groups of 8 or fewer), so each K/V byte crosses HBM once (page
+// "paged_attention_v2_triton.py": per instance, load Q, gather K/V of the
 // partition's tokens, QK^T, online softmax, weighted V; for GQA the group of
 // query heads shares the kv head).
 //
 // Data movement.  A (block, kv_head) page of either cache is one contiguous
 // run of head_size*block_size elements (4 KiB at bf16/128/16).  Each warp runs
-// its own multi-stage pipeline: its lane 0 issues cp.async.bulk copies of
-// whole K and V pages into the warp's shared-memory stages, tracked by one
-// mbarrier per stage, and the warp computes on stage i while stages i+1.. are
-// in flight.  Warp w of the CTA takes chunks w, w+WARPS, ... of the
-// partition's tokens (a chunk is 16 tokens or one page, whichever is larger).
+// its own two-stage pipeline: its lane 0 issues cp.async.bulk copies of whole
+// K and V pages into the warp's shared-memory stages, tracked by one mbarrier
+// per stage, and the warp computes on one stage while the other is in flight.
+// Warp w of the CTA takes chunks w, w+WARPS, ... of the partition's tokens (a
+// chunk is 16 tokens, 32 for one-byte caches in some instances, or one page,
+// whichever is larger).
 // Block ids are resolved once per 32 chunks: each lane loads the id of one
 // upcoming chunk from the block table and the issuing lane picks it up by
 // shuffle (the per-token global scratch of the Triton prototype on page
@@ -28,7 +30,8 @@
 // tokens; the probabilities go in as a hi + lo pair of 16-bit values
 // (movmatrix turns the score accumulator layout into the B-operand layout),
 // which keeps their rounding error near fp32.  Softmax runs in the log2
-// domain with ex2; row maxima use warp shuffles.
+// domain with ex2; row maxima use warp shuffles; a chunk in which no running
+// max grew skips the accumulator rescale (its factor would be exactly 1).
 //
 // fp32 runs the same pipeline with a CUDA-core body (no fp32 tensor path).
 //
@@ -36,14 +39,16 @@
 // "paged_attention_v2_triton.py" names kv_cache_dtype, k_scale and v_scale in
 // its wrapper, read here as vLLM's dequantisation): the pages move as bytes,
 // half the traffic of a 16-bit cache, and each lane widens the codes it needs
-// to f16 in registers for the same f16 MMAs.  A 32-bit shared load returns 4
-// codes, so both products run on permuted index orders: the key row gives
+// to f16 in registers for the same f16 MMAs.  ldmatrix hands each lane 32-bit
+// words of 4 codes, so both products run on permuted index orders: the key row gives
 // dims 4j..4j+3 to the MMA's k-slots {2j, 2j+1, 2j+8, 2j+9} (the query
 // fragments use the same order), and the score rows hold the tile's tokens in
 // the order that puts tokens 4j..4j+3 on the value product's k-slots
 // {2j, 2j+1, 2j+8, 2j+9}.  bf16 queries go to f16 with a power-of-two scale
 // per head (max |q| lands in [2^14, 2^15)), taken back out of the logit
-// scale; k_scale joins the logit scale and v_scale the epilogue.
+// scale; k_scale joins the logit scale and v_scale the epilogue; the
+// probabilities enter the value product x 256 (exact), keeping small ones
+// out of f16 subnormals.
 //
 // ALiBi (optional slopes): the logit of token t gains slope_h * (t - L + 1),
 // added in the log2 domain as slope_h * log2(e) * (t - L + 1).

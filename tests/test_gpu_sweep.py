@@ -100,6 +100,91 @@ def test_random_configuration(case):
                            f"case {case}: {dtype} D{D} bs{bs} {Hk}x{g} {mode} w{warps} {lens}")
 
 
+VARIANT_CASES = 40
+
+
+@pytest.mark.parametrize("case", range(VARIANT_CASES))
+def test_random_variant_configuration(case):
+    """Seeded sweep over the cache format (16-bit, E4M3, E5M2), ALiBi, GQA
+    groups up to 16 (sub-groups), single pass / fixed partitions / split
+    counts, block tables given as a strided 2-D table or as a flat page list
+    with an indptr, strided query/output views and warps per CTA."""
+    rng = random.Random(5000 + case)
+    dtype = rng.choice(["f16", "bf16", "bf16", "f32"])
+    kv = "auto" if dtype == "f32" else rng.choice(["auto", "fp8_e4m3", "fp8_e5m2"])
+    D = rng.choice([64, 128] if dtype == "f32" else [64, 128, 256])
+    bs = rng.choice([8, 16, 32])
+    Hk = rng.choice([1, 2])
+    g = rng.choice([1, 2, 4, 6, 8, 12, 16])
+    B = rng.randint(1, 5)
+    lens = [rng.choice([0, 1, bs, 2 * bs + 1, rng.randint(1, 900)]) for _ in range(B)]
+    if max(lens) == 0:
+        lens[0] = 7
+    alibi = rng.random() < 0.5
+    mode = rng.choice(["v1", "fixed", "splits"])
+    warps = rng.choice([0, 1, 2, 4])
+    csr = rng.random() < 0.5
+    inp = workloads.make_inputs(num_heads=Hk * g, num_kv_heads=Hk, head_size=D, block_size=bs,
+                                dtype=dtype, seq_lens=lens, seed=700 + case,
+                                bt_col_step=rng.choice([1, 2]), peaky_fraction=0.01,
+                                kv_cache_dtype=kv, k_scale=rng.choice([0.5, 1.0, 1.75]),
+                                v_scale=rng.choice([0.25, 1.0, 3.0]), alibi=alibi)
+    gd = on_device(inp)
+    kw = dict(kv_cache_dtype=kv, k_scale=inp["k_scale"], v_scale=inp["v_scale"],
+              alibi_slopes=gd["alibi_slopes"])
+    okw = dict(kw, alibi_slopes=None if not alibi else [float(v) for v in inp["alibi_slopes"]])
+    out_ref = oracle.decode_v1(inp["query"], inp["key_cache"], inp["value_cache"],
+                               inp["block_tables"], lens, inp["scale"], **okw)
+    if csr:
+        flat = [b for r in inp["block_rows"] for b in r] or [0]
+        cu = [0]
+        for r in inp["block_rows"]:
+            cu.append(cu[-1] + len(r))
+        table = torch.tensor(flat, dtype=torch.int32, device="cuda")
+        indptr = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    else:
+        table, indptr = gd["block_tables"], None
+    q = _strided_like(gd["query"], rng)
+    out = _strided_like(torch.zeros_like(gd["query"]), rng)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.set_attention_warps(warps)
+    try:
+        if mode == "v1":
+            pkv.paged_attention_decode(out, q, gd["key_cache"], gd["value_cache"], table,
+                                       gd["seq_lens"], inp["scale"], kv_indptr=indptr,
+                                       err_flag=err, **kw)
+        else:
+            Bq, H, _ = q.shape
+            cap = inp["max_blocks_per_seq"] * bs
+            if mode == "fixed":
+                P = bs * rng.choice([1, 2, 4, 32])
+                maxP = -(-cap // P)
+                splits = None
+            else:
+                P = 512
+                maxP = rng.randint(1, 12)
+                splits = torch.tensor([rng.randint(1, maxP) for _ in range(B)], dtype=torch.int32,
+                                      device="cuda")
+            tmp = torch.empty(Bq, H, maxP, D, dtype=torch.float32, device="cuda")
+            es = torch.empty(Bq, H, maxP, dtype=torch.float32, device="cuda")
+            ml = torch.empty(Bq, H, maxP, dtype=torch.float32, device="cuda")
+            pkv.paged_attention_v2_partition(tmp, es, ml, q, gd["key_cache"], gd["value_cache"],
+                                             table, gd["seq_lens"], inp["scale"],
+                                             partition_size=P, num_kv_splits=splits,
+                                             kv_indptr=indptr, err_flag=err,
+                                             max_blocks_per_seq=inp["max_blocks_per_seq"],
+                                             **kw)
+            pkv.paged_attention_v2_reduce(out, tmp, es, ml, gd["seq_lens"], partition_size=P,
+                                          num_kv_splits=splits, block_size=bs, err_flag=err)
+    finally:
+        pkv.set_attention_warps(0)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, out_ref, DT[dtype],
+                           f"variant case {case}: {dtype}/{kv} D{D} bs{bs} {Hk}x{g} alibi={alibi} "
+                           f"{mode} csr={csr} w{warps} {lens}")
+
+
 def test_offsets_beyond_four_gigabytes():
     """Sequence 0 lives in the last blocks of a cache of 300,000 blocks
     (each tensor 9.8 GB; its element offsets exceed 2^32)."""

@@ -177,3 +177,36 @@ def test_alibi_slopes_must_be_float32_per_head():
     with pytest.raises(ValueError):
         run_v1(g)
     assert not math.isnan(float(inp["alibi_slopes"][0]))
+
+
+@pytest.mark.parametrize("warps", [0, 2])
+def test_fp8_copy_wait_timeout_is_reported_and_the_context_survives(warps):
+    """The fp8 body's bounded waits: with the test hook every stage expects 16
+    bytes that never arrive, the waits run out (20 ms), the kernel reports
+    PKV_ERRF_TIMEOUT and finishes, and the next launch is correct."""
+    inp = workloads.make_inputs(num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                                dtype="bf16", seq_lens=[64, 300], seed=51,
+                                kv_cache_dtype="fp8_e4m3", k_scale=0.5, v_scale=2.0)
+    g = on_device(inp)
+    ref = oracle.decode_v1(inp["query"], inp["key_cache"], inp["value_cache"],
+                           inp["block_tables"], inp["seq_lens_list"], inp["scale"],
+                           **oracle_kwargs(inp))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.set_attention_warps(warps)
+    pkv.set_wait_limit_ns(20_000_000)
+    pkv._test_set_unarrived_bytes(16)
+    try:
+        run_v1(g, err=err)
+        torch.cuda.synchronize()
+    finally:
+        pkv._test_set_unarrived_bytes(0)
+        pkv.set_wait_limit_ns(0)
+    try:
+        assert int(err.item()) & pkv.PKV_ERRF_TIMEOUT
+        err.zero_()
+        out = run_v1(g, err=err)
+        torch.cuda.synchronize()
+    finally:
+        pkv.set_attention_warps(0)
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, torch.bfloat16, f"fp8 after timeout, warps {warps}")
