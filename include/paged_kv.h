@@ -140,7 +140,7 @@ typedef struct {
   const float *alibi_slopes;
 } pkv_decode_args_t;
 
-/* Library version string, e.g. "paged_kv 0.1.0 sm_103a". */
+/* Library version string, e.g. "paged_kv 0.2.0 sm_103a". */
 const char *pkv_version(void);
 /* Static description of a status code. */
 const char *pkv_status_string(pkv_status_t status);

@@ -177,7 +177,7 @@ int pick_warps(const pkv_decode_args_t *a, int64_t units, Pass pass, int partiti
 
 extern "C" {
 
-const char *pkv_version(void) { return "paged_kv 0.1.0 sm_103a"; }
+const char *pkv_version(void) { return "paged_kv 0.2.0 sm_103a"; }
 
 const char *pkv_status_string(pkv_status_t s) {
   switch (s) {
