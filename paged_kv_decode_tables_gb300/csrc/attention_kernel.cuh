@@ -783,6 +783,18 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       const int pb = int(t0 + c * CH) - L + 1;
       const float *kf = reinterpret_cast<const float *>(wbase + st * Cfg::kStageBytes);
       const float *vf = kf + CH * D;
+      // The chunk's tokens accumulate into chunk-local sums (cacc, cl) while
+      // cs collects the chunk's rescale factors for the running ones, which
+      // then take one addition per chunk instead of one per token: the fp32
+      // rounding of a long sequence grows with its chunk count, not its length.
+      float cacc[kMaxGroup][DL], cl[kMaxGroup], cs[kMaxGroup];
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+#pragma unroll
+        for (int i2 = 0; i2 < DL; ++i2) cacc[h][i2] = 0.f;
+        cl[h] = 0.f;
+        cs[h] = 1.f;
+      }
       for (int tau = 0; tau < nv; ++tau) {
         const int pg = tau / BS, slot = tau % BS;
         float kv[DL], vv[DL];
@@ -805,12 +817,19 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
             const float mn = fmaxf(m_run[h], xs);
             const float a = ex2(m_run[h] - mn);
             const float pe = ex2(xs - mn);
-            l_run[h] = l_run[h] * a + pe;
+            cl[h] = cl[h] * a + pe;
+            cs[h] *= a;
 #pragma unroll
-            for (int i2 = 0; i2 < DL; ++i2) acc[h][i2] = fmaf(acc[h][i2], a, pe * vv[i2]);
+            for (int i2 = 0; i2 < DL; ++i2) cacc[h][i2] = fmaf(cacc[h][i2], a, pe * vv[i2]);
             m_run[h] = mn;
           }
         }
+      }
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+        l_run[h] = fmaf(l_run[h], cs[h], cl[h]);
+#pragma unroll
+        for (int i2 = 0; i2 < DL; ++i2) acc[h][i2] = fmaf(acc[h][i2], cs[h], cacc[h][i2]);
       }
       __syncwarp();
       if (issued < my_n) issue_next();

@@ -100,10 +100,12 @@ def test_random_configuration(case):
                            f"case {case}: {dtype} D{D} bs{bs} {Hk}x{g} {mode} w{warps} {lens}")
 
 
-VARIANT_CASES = 40
+# 40 seeds, plus two that once exposed fp32 rounding growing with the length
+# of a warp's sequential accumulation (one warp, 800-token sequences).
+VARIANT_CASES = list(range(40)) + [179, 228]
 
 
-@pytest.mark.parametrize("case", range(VARIANT_CASES))
+@pytest.mark.parametrize("case", VARIANT_CASES)
 def test_random_variant_configuration(case):
     """Seeded sweep over the cache format (16-bit, E4M3, E5M2), ALiBi, GQA
     groups up to 16 (sub-groups), single pass / fixed partitions / split
