@@ -187,36 +187,47 @@ def test_random_variant_configuration(case):
                            f"{mode} csr={csr} w{warps} {lens}")
 
 
-def test_offsets_beyond_four_gigabytes():
-    """Sequence 0 lives in the last blocks of a cache of 300,000 blocks
-    (each tensor 9.8 GB; its element offsets exceed 2^32)."""
-    NB, Hk, D, bs = 300_000, 8, 128, 16
+@pytest.mark.parametrize("kv,NB", [("auto", 300_000), ("fp8_e4m3", 600_000)])
+def test_offsets_beyond_four_gigabytes(kv, NB):
+    """Sequence 0 lives in the last blocks of a cache whose byte offsets exceed
+    2^32 (bf16: 300,000 blocks, 9.8 GB per tensor; fp8: 600,000 blocks,
+    9.8 GB of one-byte codes per tensor)."""
+    Hk, D, bs = 8, 128, 16
     lens = [64, 100, 37]
     last = list(range(NB - 4, NB))
     inp = workloads.make_inputs(num_heads=32, num_kv_heads=Hk, head_size=D, block_size=bs,
                                 dtype="bf16", seq_lens=lens, num_blocks=NB, first_row=last[::-1],
-                                seed=7, device="cuda")
-    assert int(inp["block_tables"][0].max()) * Hk * D * bs > 2 ** 32
+                                seed=7, device="cuda", kv_cache_dtype=kv, k_scale=0.5,
+                                v_scale=2.0)
+    elem = inp["key_cache"].element_size()
+    assert int(inp["block_tables"][0].max()) * Hk * D * bs * elem > 2 ** 33
     out = torch.empty_like(inp["query"])
     pkv.paged_attention_decode(out, inp["query"], inp["key_cache"], inp["value_cache"],
-                               inp["block_tables"], inp["seq_lens"], inp["scale"])
+                               inp["block_tables"], inp["seq_lens"], inp["scale"],
+                               kv_cache_dtype=kv, k_scale=0.5, v_scale=2.0)
     torch.cuda.synchronize()
     q, kc, vc, bt, ls = bench.oracle_sample_inputs(inp, [0, 1, 2])
-    ref = oracle.decode_v1(q, kc, vc, bt, ls, inp["scale"])
-    assert_attention_close(out, ref, torch.bfloat16, "offsets beyond 2^32")
+    ref = oracle.decode_v1(q, kc, vc, bt, ls, inp["scale"], kv_cache_dtype=kv, k_scale=0.5,
+                           v_scale=2.0)
+    assert_attention_close(out, ref, torch.bfloat16, f"offsets beyond 2^32 ({kv})")
     del inp
     torch.cuda.empty_cache()
 
 
-def test_single_pass_128k_tokens():
+@pytest.mark.parametrize("kv,alibi", [("auto", False), ("fp8_e5m2", True)])
+def test_single_pass_128k_tokens(kv, alibi):
     lens = [131072]
     inp = workloads.make_inputs(num_heads=8, num_kv_heads=1, head_size=128, block_size=16,
                                 dtype="bf16", seq_lens=lens, seed=8, device="cuda",
-                                peaky_fraction=0.01)
+                                peaky_fraction=0.01, kv_cache_dtype=kv, alibi=alibi)
+    if alibi:
+        inp["alibi_slopes"] = inp["alibi_slopes"] * 1e-4  # keep far tokens in play
     out = torch.empty_like(inp["query"])
     pkv.paged_attention_decode(out, inp["query"], inp["key_cache"], inp["value_cache"],
-                               inp["block_tables"], inp["seq_lens"], inp["scale"])
+                               inp["block_tables"], inp["seq_lens"], inp["scale"],
+                               kv_cache_dtype=kv, alibi_slopes=inp["alibi_slopes"])
     torch.cuda.synchronize()
     q, kc, vc, bt, ls = bench.oracle_sample_inputs(inp, [0])
-    ref = oracle.decode_v1(q, kc, vc, bt, ls, inp["scale"])
-    assert_attention_close(out, ref, torch.bfloat16, "128k single pass")
+    sl = None if not alibi else [float(v) for v in inp["alibi_slopes"].cpu()]
+    ref = oracle.decode_v1(q, kc, vc, bt, ls, inp["scale"], kv_cache_dtype=kv, alibi_slopes=sl)
+    assert_attention_close(out, ref, torch.bfloat16, f"128k single pass ({kv}, alibi={alibi})")
