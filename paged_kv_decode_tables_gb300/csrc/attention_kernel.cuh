@@ -127,14 +127,19 @@ struct AttnCfg {
   static_assert(kHalfStage % 16 == 0 && kPageBytes % 16 == 0, "bulk copies need 16 B");
 };
 
-// CTAs per SM an instance is compiled to keep resident (0: no floor).
-// Measured for fp8 caches with two warps per CTA up to head size 128: a floor
-// of 10 CTAs (96 registers, a few bytes of spill) beats the 8 that 127
-// registers allow (ragged batch 360 -> 347 us); 9 CTAs gain nothing, and one
-// or four warps per CTA lose.
+// CTAs per SM an instance is compiled to keep resident (0: no floor), all
+// measured on fp8 caches (elsewhere floors lose):
+// - head size 128, two warps per CTA: 10 CTAs (96 registers, a few bytes of
+//   spill) beat the 8 that 127 registers allow (ragged batch 360 -> 347 us);
+//   9 CTAs gain nothing, and one or four warps per CTA lose;
+// - head size 64: 14 two-warp CTAs (ragged 480 -> 459 us) and 6 four-warp
+//   CTAs (GQA single pass 128 -> 124 us).
 template <typename KV, int D, int WARPS>
 constexpr int resident_ctas() {
-  return (is_fp8<KV>::value && D <= 128 && WARPS == 2) ? 10 : 0;
+  if constexpr (!is_fp8<KV>::value) return 0;
+  if constexpr (D == 64) return WARPS == 2 ? 14 : (WARPS == 4 ? 6 : 0);
+  if constexpr (D == 128) return WARPS == 2 ? 10 : 0;
+  return 0;
 }
 
 template <typename T, typename KV, int D, int BS, int WARPS>
