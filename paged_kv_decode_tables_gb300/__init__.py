@@ -24,6 +24,7 @@ __all__ = [
     "lib_path",
     "version",
     "set_attention_warps",
+    "set_wait_limit_ns",
     "paged_attention_decode",
     "paged_attention_v2_partition",
     "paged_attention_v2_reduce",
@@ -207,7 +208,8 @@ def _stream(stream) -> int:
 
 
 def set_attention_warps(warps: int) -> None:
-    """Force warps per CTA (1 or 4) for the attention kernels; 0 restores the default."""
+    """Force warps per CTA (1, 2 or 4) for the attention kernels where that
+    instance exists; 0 restores the measured per-call choice."""
     _check(lib().pkv_set_attention_warps(int(warps)), "pkv_set_attention_warps")
 
 
@@ -311,7 +313,12 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
                            kv_cache_dtype: str = "auto", k_scale: float = 1.0,
                            v_scale: float = 1.0, alibi_slopes: Optional[torch.Tensor] = None,
                            stream=None) -> None:
-    """Single-pass decode into ``out [num_seqs, num_heads, head_size]`` (query's dtype)."""
+    """Single-pass decode into ``out [num_seqs, num_heads, head_size]`` (query's dtype).
+
+    ``kv_cache_dtype`` ("auto", "fp8", "fp8_e4m3", "fp8_e5m2") with uint8 code
+    caches, or float8 caches under "auto", selects an fp8 cache dequantised as
+    ``code * k_scale`` / ``code * v_scale``; ``alibi_slopes`` (float32
+    ``[num_heads]``) adds ``slope_h * (t - seq_len + 1)`` to the logits."""
     _cuda(out, "out")
     if out.dtype != query.dtype or tuple(out.shape) != tuple(query.shape):
         raise ValueError("out must match query's shape and dtype")
