@@ -8,11 +8,14 @@
 //   page_table[i, c] = page_index >> SHIFT                     (SHIFT = log2(page_size))
 //   swa_page_table[i, c] = full_to_swa_mapping[page_index] >> SHIFT   (optional)
 //
-// Blocks [0, B * chunks) gather one 2048-column chunk of one request row each
-// (eight columns per thread, their loads issued together); the last block
-// computes the lengths and the scan with warp shuffles, 256 at a time.  Row and column indices into the
-// token pool and the mapping are bounds-checked: an out-of-range index writes
-// 0 and sets PKV_ERRF_INDPTR.
+// Blocks [0, B * chunks) gather one chunk of one request row each (the last
+// block computes the lengths and the scan with warp shuffles, 256 at a time).
+// General form: 2048-column chunks, eight columns per thread, their loads
+// issued together.  Page size 1 without the sliding-window table over
+// unit-stride, 16-byte aligned rows is a plain row copy: 4096-column chunks,
+// sixteen columns per thread moved as four 16-byte loads and stores.  Row and
+// column indices into the token pool and the mapping are bounds-checked: an
+// out-of-range index writes 0 and sets PKV_ERRF_INDPTR.
 #include <cuda_runtime.h>
 
 #include "../../include/paged_kv.h"
@@ -26,7 +29,55 @@ namespace {
 constexpr int kCols = 256;                           // threads per block
 constexpr int kPerThread = 8;                        // columns per thread
 constexpr int kChunkCols = kCols * kPerThread;       // columns per block
+constexpr int kVecPerThread = 4;                     // row copy: int4 per thread
+constexpr int kVecChunkCols = kCols * kVecPerThread * 4;
 
+// Page size 1, no sliding-window table: page_table row i = the first
+// max_seq_pages entries of token-pool row req_pool_indices[i], 16 bytes at a
+// time (columns past the pool's width or a bad row write 0 and flag).
+__device__ __forceinline__ void copy_row_vec(const pkv_decode_metadata_args_t &a, int i, int chunk,
+                                             int tid) {
+  const int64_t row = a.req_pool_indices[int64_t(i) * a.req_pool_indices_stride];
+  const bool row_ok = row >= 0 && row < a.req_to_token_rows;
+  const int32_t *src = a.req_to_token + (row_ok ? row : 0) * a.req_to_token_stride[0];
+  int32_t *dst = a.page_table + int64_t(i) * a.page_table_stride[0];
+  const int cbase = chunk * kVecChunkCols + 4 * tid;
+  int4 v[kVecPerThread];
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k) {
+    const int c = cbase + k * (4 * kCols);
+    v[k] = make_int4(0, 0, 0, 0);
+    if (c + 3 < a.max_seq_pages && row_ok && int64_t(c) + 3 < a.req_to_token_cols) {
+      v[k] = __ldcs(reinterpret_cast<const int4 *>(src + c));
+    } else {
+      int e[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (c + j < a.max_seq_pages) {
+          if (row_ok && int64_t(c) + j < a.req_to_token_cols)
+            e[j] = src[c + j];
+          else
+            flag_error(a.err_flag, 8u);
+        }
+      }
+      v[k] = make_int4(e[0], e[1], e[2], e[3]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k) {
+    const int c = cbase + k * (4 * kCols);
+    if (c + 3 < a.max_seq_pages) {
+      __stcs(reinterpret_cast<int4 *>(dst + c), v[k]);
+    } else {
+      const int e[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (c + j < a.max_seq_pages) dst[c + j] = e[j];
+    }
+  }
+}
+
+template <bool kRowCopy>
 __global__ void __launch_bounds__(kCols) decode_metadata_kernel(const pkv_decode_metadata_args_t a,
                                                                 int shift, int chunks) {
   grid_dependency_wait();
@@ -73,6 +124,10 @@ __global__ void __launch_bounds__(kCols) decode_metadata_kernel(const pkv_decode
     return;
   }
   const int i = int(blockIdx.x / unsigned(chunks));
+  if constexpr (kRowCopy) {
+    copy_row_vec(a, i, int(blockIdx.x % unsigned(chunks)), tid);
+    return;
+  }
   const int c0 = int(blockIdx.x % unsigned(chunks)) * kChunkCols + tid;
   const int64_t row = a.req_pool_indices[int64_t(i) * a.req_pool_indices_stride];
   const bool row_ok = row >= 0 && row < a.req_to_token_rows;
@@ -143,12 +198,21 @@ extern "C" pkv_status_t normal_decode_set_metadata(const pkv_decode_metadata_arg
     return PKV_ERR_INVALID_ARG;
   int shift = 0;
   while ((1 << shift) < a->page_size) ++shift;
-  const int chunks = (a->max_seq_pages + pkv::kChunkCols - 1) / pkv::kChunkCols;
+  auto aligned16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool row_copy = shift == 0 && a->swa_page_table == nullptr && a->max_seq_pages > 0 &&
+                        a->req_to_token_stride[1] == 1 && a->page_table_stride[1] == 1 &&
+                        a->req_to_token_stride[0] % 4 == 0 && a->page_table_stride[0] % 4 == 0 &&
+                        aligned16(a->req_to_token) && aligned16(a->page_table);
+  const int chunk_cols = row_copy ? pkv::kVecChunkCols : pkv::kChunkCols;
+  const int chunks = (a->max_seq_pages + chunk_cols - 1) / chunk_cols;
   const int64_t blocks = int64_t(a->batch_size) * chunks + 1;
   if (blocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
-  return pkv::launch_programmatic(pkv::decode_metadata_kernel, dim3(unsigned(blocks)),
-                                  dim3(pkv::kCols), 0, reinterpret_cast<cudaStream_t>(stream), *a,
-                                  shift, chunks) == cudaSuccess
-             ? PKV_OK
-             : PKV_ERR_CUDA;
+  const cudaError_t e =
+      row_copy ? pkv::launch_programmatic(pkv::decode_metadata_kernel<true>, dim3(unsigned(blocks)),
+                                          dim3(pkv::kCols), 0,
+                                          reinterpret_cast<cudaStream_t>(stream), *a, shift, chunks)
+               : pkv::launch_programmatic(pkv::decode_metadata_kernel<false>,
+                                          dim3(unsigned(blocks)), dim3(pkv::kCols), 0,
+                                          reinterpret_cast<cudaStream_t>(stream), *a, shift, chunks);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

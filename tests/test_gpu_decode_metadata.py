@@ -97,3 +97,53 @@ def test_decode_metadata_flags_bad_pool_rows():
     assert int(err.item()) & pkv.PKV_ERRF_INDPTR
     assert pt[0].cpu().tolist() == [4, 5, 6, 7]  # row 1: tokens 8,10,12,14 >> 1
     assert pt[1].cpu().tolist() == [0, 0, 0, 0]
+
+
+@pytest.mark.parametrize("B,msp", [(3, 4), (5, 300), (2, 4096), (4, 4099), (3, 8195), (600, 37)])
+def test_decode_metadata_row_copy_path(B, msp):
+    """Page size 1, no sliding-window table, unit-stride 16-byte aligned rows:
+    the 16-byte row copy, including a ragged tail inside a padded row."""
+    g = torch.Generator().manual_seed(B * 7 + msp)
+    width = -(-msp // 4) * 4
+    rt = torch.randint(0, 1 << 30, (B + 4, width + 8), generator=g, dtype=torch.int32)
+    pool = torch.randperm(B + 4, generator=g)[:B].to(torch.int64)
+    lens = torch.randint(0, msp + 1, (B,), generator=g, dtype=torch.int64)
+    dev = "cuda"
+    cache = torch.empty(B, dtype=torch.int32, device=dev)
+    cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    pt_store = torch.full((B, width + 4), -9, dtype=torch.int32, device=dev)
+    pt = pt_store[:, :msp]
+    assert pt.stride(0) % 4 == 0 and pt.stride(1) == 1
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.normal_decode_set_metadata(cache, cu, pt, rt.to(dev), pool.to(dev), lens.to(dev),
+                                   seq_len_delta=1, page_size=1, max_seq_pages=msp, err_flag=err)
+    want = oracle.decode_set_metadata(lens.tolist(), rt, pool.tolist(), msp, 1, 1)
+    torch.cuda.synchronize()
+    assert cache.cpu().tolist() == want[0]
+    assert cu.cpu().tolist() == want[1]
+    assert pt.cpu().tolist() == want[2]
+    assert bool((pt_store[:, msp:] == -9).all())
+    assert int(err.item()) == 0
+
+
+def test_decode_metadata_row_copy_short_and_bad_rows():
+    """Row copy with pool rows narrower than max_seq_pages (columns past the
+    width write 0) and a pool index outside the pool (the row writes 0):
+    both flagged."""
+    dev = "cuda"
+    rt = torch.arange(3 * 100, dtype=torch.int32, device=dev).view(3, 100)
+    pool = torch.tensor([2, 7, 0], dtype=torch.int64, device=dev)  # 7 is outside the pool
+    lens = torch.tensor([5, 6, 7], dtype=torch.int64, device=dev)
+    cache = torch.empty(3, dtype=torch.int32, device=dev)
+    cu = torch.empty(4, dtype=torch.int32, device=dev)
+    pt = torch.full((3, 132), -1, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.normal_decode_set_metadata(cache, cu, pt, rt, pool, lens, seq_len_delta=0, page_size=1,
+                                   max_seq_pages=130, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.PKV_ERRF_INDPTR
+    got = pt.cpu()
+    assert got[0, :100].tolist() == list(range(200, 300)) and got[0, 100:130].tolist() == [0] * 30
+    assert got[1, :130].tolist() == [0] * 130
+    assert got[2, :100].tolist() == list(range(0, 100)) and got[2, 100:130].tolist() == [0] * 30
+    assert got[:, 130:].tolist() == [[-1, -1]] * 3
