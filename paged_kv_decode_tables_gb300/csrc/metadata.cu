@@ -7,8 +7,8 @@
 // compute_num_kv_splits: sglang metadata.py, get_num_kv_splits_triton.  One
 //   CTA: block-wide max/min of the lengths, the split formula evaluated once,
 //   then every thread writes its sequences' counts.
-// prepare_decode_metadata: both of the above in one launch (a warp per table
-//   row, plus one CTA for the split counts).
+// prepare_decode_metadata: both of the above in one launch (a warp per
+//   256-column segment of a table row, plus one CTA for the split counts).
 #include "metadata.cuh"
 #include "pkv_launch.cuh"
 
@@ -18,7 +18,8 @@ namespace {
 
 constexpr int kCopyThreads = 128;
 constexpr int kSplitThreads = 1024;
-constexpr int kFusedThreads = 256;  // fused launch: a warp per table row, one CTA for the splits
+constexpr int kFusedThreads = 256;  // fused launch: a warp per row segment, one CTA for the splits
+constexpr int kSegCols = 256;       // columns of a row segment: eight per lane
 
 __device__ __forceinline__ int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -42,6 +43,43 @@ __device__ __forceinline__ void copy_row(int32_t *__restrict__ out, int64_t capa
   const int32_t *row = bt + int64_t(i) * s0;
   int32_t *dst = out + start;
   for (int64_t j = tid; j < n; j += nthreads) dst[j] = __ldg(row + j * s1);
+}
+
+// Columns [seg * kSegCols, (seg + 1) * kSegCols) of row i of the page-index
+// copy, one warp, the lane's eight loads issued before its stores (the same
+// checks as copy_row; a bad indptr row is flagged by its segment 0).
+__device__ __forceinline__ void copy_row_segment(int32_t *__restrict__ out, int64_t capacity,
+                                                 const int32_t *__restrict__ bt, int32_t num_cols,
+                                                 int64_t s0, int64_t s1,
+                                                 const int32_t *__restrict__ cu, int32_t *err,
+                                                 int i, int seg, int lane) {
+  const int64_t start = cu[i];
+  int64_t n = int64_t(cu[i + 1]) - start;
+  const bool report = seg == 0 && lane == 0;
+  if (start < 0 || n < 0 || n > num_cols) {
+    if (report) flag_error(err, 8u);
+    if (start < 0) return;
+    n = n < 0 ? 0 : num_cols;
+  }
+  if (start + n > capacity) {
+    if (report) flag_error(err, 8u);
+    n = capacity > start ? capacity - start : 0;
+  }
+  const int64_t j0 = int64_t(seg) * kSegCols;
+  if (j0 >= n) return;
+  const int32_t *row = bt + int64_t(i) * s0;
+  int32_t v[kSegCols / 32];
+#pragma unroll
+  for (int k = 0; k < kSegCols / 32; ++k) {
+    const int64_t j = j0 + lane + 32 * k;
+    v[k] = j < n ? __ldg(row + j * s1) : 0;
+  }
+  int32_t *dst = out + start;
+#pragma unroll
+  for (int k = 0; k < kSegCols / 32; ++k) {
+    const int64_t j = j0 + lane + 32 * k;
+    if (j < n) dst[j] = v[k];
+  }
 }
 
 // The split-count heuristic on one CTA of THREADS threads.
@@ -127,14 +165,16 @@ __global__ void __launch_bounds__(kSplitThreads)
 }
 
 // Both metadata steps in one grid: blocks [0, copy_blocks) copy table rows (a
-// warp per row), the last block computes the split counts.
+// warp per 256-column segment, so long rows do not set the grid's length),
+// the last block computes the split counts.
 __global__ void __launch_bounds__(kFusedThreads)
     decode_metadata_kernel(int32_t *__restrict__ page_indices, int64_t capacity,
                            const int32_t *__restrict__ bt, int32_t num_cols, int64_t s0,
                            int64_t s1, const int32_t *__restrict__ cu, int32_t num_reqs,
                            int32_t *__restrict__ splits, const int32_t *__restrict__ seq_lens,
                            int32_t num_group, int32_t num_head, int32_t num_kv_head,
-                           int32_t max_kv_splits, int32_t core_count, int32_t *err) {
+                           int32_t max_kv_splits, int32_t core_count, int32_t *err,
+                           int32_t segs) {
   grid_dependency_wait();
   allow_dependent_launch();
   if (blockIdx.x == gridDim.x - 1) {
@@ -142,9 +182,11 @@ __global__ void __launch_bounds__(kFusedThreads)
                                 max_kv_splits, core_count);
     return;
   }
-  const int row = blockIdx.x * (kFusedThreads / 32) + (threadIdx.x >> 5);
+  const int64_t w = int64_t(blockIdx.x) * (kFusedThreads / 32) + (threadIdx.x >> 5);
+  const int64_t row = w / segs;
   if (row < num_reqs)
-    copy_row(page_indices, capacity, bt, num_cols, s0, s1, cu, err, row, threadIdx.x & 31, 32);
+    copy_row_segment(page_indices, capacity, bt, num_cols, s0, s1, cu, err, int(row),
+                     int(w - row * segs), threadIdx.x & 31);
 }
 
 }  // namespace
@@ -178,12 +220,15 @@ pkv_status_t launch_decode_metadata(int32_t *page_indices, int64_t capacity,
                                     int32_t *splits, const int32_t *seq_lens, int32_t num_group,
                                     int32_t num_head, int32_t num_kv_head, int32_t max_kv_splits,
                                     int32_t core_count, int32_t *err, cudaStream_t stream) {
-  const int rows_per_block = kFusedThreads / 32;
-  const int copy_blocks = (num_reqs + rows_per_block - 1) / rows_per_block;
-  return launch_programmatic(decode_metadata_kernel, dim3(copy_blocks + 1), dim3(kFusedThreads), 0,
-                             stream, page_indices, capacity, block_table, num_cols, s0, s1, cu,
-                             num_reqs, splits, seq_lens, num_group, num_head, num_kv_head,
-                             max_kv_splits, core_count, err) == cudaSuccess
+  const int warps_per_block = kFusedThreads / 32;
+  const int32_t segs = num_cols > 0 ? (num_cols + kSegCols - 1) / kSegCols : 1;
+  const int64_t copy_blocks = (int64_t(num_reqs) * segs + warps_per_block - 1) / warps_per_block;
+  if (copy_blocks + 1 > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+  return launch_programmatic(decode_metadata_kernel, dim3(unsigned(copy_blocks + 1)),
+                             dim3(kFusedThreads), 0, stream, page_indices, capacity, block_table,
+                             num_cols, s0, s1, cu, num_reqs, splits, seq_lens, num_group,
+                             num_head, num_kv_head, max_kv_splits, core_count, err,
+                             segs) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
 }

@@ -121,12 +121,14 @@ def test_num_kv_splits_float32_step_exhaustive():
     assert not bad, bad[:10]
 
 
+@pytest.mark.parametrize("W", [300, 2048])
 @pytest.mark.parametrize("col_step", [1, 2])
 @pytest.mark.parametrize("R", [1, 7, 9, 512, 1000])
-def test_fused_metadata_equals_both_steps(R, col_step):
-    """prepare_decode_metadata == copy_page_indices + compute_num_kv_splits, bit for bit."""
-    g = torch.Generator().manual_seed(R + 17 * col_step)
-    W = 300
+def test_fused_metadata_equals_both_steps(R, col_step, W):
+    """prepare_decode_metadata == copy_page_indices + compute_num_kv_splits, bit
+    for bit (rows of up to 300 and 2048 columns: two and eight 256-column
+    segments)."""
+    g = torch.Generator().manual_seed(R + 17 * col_step + W)
     storage = torch.randint(0, 1 << 20, (R, W * col_step), generator=g, dtype=torch.int32)
     bt = storage[:, ::col_step]
     lens = torch.randint(0, W * 16 + 1, (R,), generator=g)
@@ -147,3 +149,28 @@ def test_fused_metadata_equals_both_steps(R, col_step):
     assert pi.cpu().tolist() == oracle.copy_page_indices(bt, cu, cap, fill=-3)
     assert splits.cpu().tolist() == oracle.num_kv_splits(lens.tolist(), 1, 32, 8, 16, 148)
     assert int(err.item()) == 0
+
+
+def test_fused_metadata_flags_bad_indptr_rows():
+    """The fused copy applies copy_page_indices' checks: a row longer than the
+    table is cut to its width, a negative start skips the row, a row past the
+    output capacity is cut to it; each is flagged."""
+    W = 600
+    bt = torch.arange(4 * W, dtype=torch.int32).view(4, W)
+    cu = [0, 700, 710, 720, 760]        # row 0 claims 700 > W columns
+    cap = 745                           # row 3 ends past the capacity
+    pi = torch.full((cap,), -3, dtype=torch.int32, device="cuda")
+    splits = torch.empty(4, dtype=torch.int32, device="cuda")
+    lens = torch.tensor([700 * 16, 10 * 16, 10 * 16, 40 * 16], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.prepare_decode_metadata(pi, bt.cuda(), torch.tensor(cu, dtype=torch.int32, device="cuda"),
+                                splits, lens, num_group=1, num_head=32, num_kv_head=8,
+                                max_kv_splits=16, device_core_count=148, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.PKV_ERRF_INDPTR
+    got = pi.cpu().tolist()
+    assert got[0:W] == bt[0].tolist()             # row 0 cut to the table width
+    assert got[W:700] == [-3] * (700 - W)         # nothing past it
+    assert got[700:710] == bt[1, :10].tolist()
+    assert got[710:720] == bt[2, :10].tolist()
+    assert got[720:745] == bt[3, :25].tolist()    # row 3 cut at the capacity
