@@ -210,3 +210,33 @@ def test_binding_refuses_host_tensors():
         pkv.paged_attention_decode(q, q, torch.zeros(1, 1, 16, 8, 4), torch.zeros(1, 1, 64, 8),
                                    torch.zeros(1, 1, dtype=torch.int32),
                                    torch.zeros(1, dtype=torch.int32), 0.1)
+
+
+def test_binding_resolves_the_cache_format():
+    """kv_cache_dtype names and float8 tensor types map to pkv_kv_cache_dtype_t;
+    contradictions and wrong element types are refused (host-side only)."""
+    import torch
+
+    import paged_kv_decode_tables_gb300 as pkv
+    q = torch.zeros(1, 1, 16, dtype=torch.bfloat16)
+    u8 = torch.zeros(1, 1, 1, 4, 16, dtype=torch.uint8)
+    e4 = u8.view(torch.float8_e4m3fn)
+    e5 = u8.view(torch.float8_e5m2)
+    bf = torch.zeros(1, 1, 2, 4, 8, dtype=torch.bfloat16)
+    assert pkv._kv_cache_code(bf, bf, q, "auto") == 0
+    assert pkv._kv_cache_code(u8, u8, q, "fp8") == 1
+    assert pkv._kv_cache_code(u8, u8, q, "fp8_e4m3") == 1
+    assert pkv._kv_cache_code(u8, u8, q, "fp8_e5m2") == 2
+    assert pkv._kv_cache_code(e4, e4, q, "auto") == 1
+    assert pkv._kv_cache_code(e5, e5, q, "auto") == 2
+    assert pkv._kv_cache_code(e5, e5, q, "fp8_e5m2") == 2
+    with pytest.raises(ValueError):
+        pkv._kv_cache_code(e4, e4, q, "fp8_e5m2")      # contradicts the tensor type
+    with pytest.raises(ValueError):
+        pkv._kv_cache_code(u8, u8, q, "auto")          # codes need a format name
+    with pytest.raises(ValueError):
+        pkv._kv_cache_code(bf, bf, q, "fp8")           # fp8 caches are codes
+    with pytest.raises(ValueError):
+        pkv._kv_cache_code(u8, u8, q, "int8")          # unknown name
+    with pytest.raises(ValueError):
+        pkv._kv_cache_code(u8, e4, q, "fp8")           # key and value differ
