@@ -162,6 +162,36 @@ class ClockSampler:
 
 # --------------------------------------------------------- the decode step --
 
+def kv_bytes_of(inp) -> int:
+    """K/V bytes one step reads: every token of every sequence, per kv head."""
+    kc = inp["key_cache"]
+    return sum(inp["seq_lens_list"]) * kc.shape[1] * 2 * inp["query"].shape[2] * kc.element_size()
+
+
+def flushes_l2(inp) -> bool:
+    """Workloads whose K/V is not far larger than L2 get L2 flushed between steps."""
+    return kv_bytes_of(inp) < 4 * L2_BYTES
+
+
+def workload_config(inp, world: int = 1) -> dict:
+    """The workload's identifying configuration: the same dict in both arms."""
+    spec = inp["spec"]
+    B, H, D = inp["query"].shape
+    kc = inp["key_cache"]
+    kvb = kv_bytes_of(inp)
+    return {
+        "workload": spec.name,
+        "description": spec.description,
+        "num_seqs": B, "num_heads": H, "num_kv_heads": kc.shape[1],
+        "head_size": D, "block_size": kc.shape[3],
+        "kv_cache_dtype": spec.kv_cache_dtype, "alibi": spec.alibi,
+        "total_tokens": sum(inp["seq_lens_list"]), "kv_bytes_per_step": kvb,
+        "l2": ("flushed between steps (512 MB write)" if flushes_l2(inp) else
+               f"inputs larger than L2: {kvb / 1e9:.2f} GB of K/V per step"),
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
 class DecodeStep:
     """Device buffers of one workload and the launches of one step, issued
     straight through the C ABI with argument structs prepared once."""
@@ -305,24 +335,37 @@ class DecodeStep:
                 "reduce")
             mark("paged_attention_v2_reduce", 1)
 
+    def config(self, world: int = 1) -> dict:
+        return workload_config(self.inp, world)
+
     def host_inputs(self):
-        """Pinned host copies of the per-step inputs (query, lengths, table,
-        indptr) and a pinned host buffer for the result."""
+        """Pinned host copies of the per-step inputs (query, lengths, the live
+        block-table view packed row by row, indptr) and a pinned host buffer for
+        the result.  Only the table's view is sent, not its backing storage (a
+        stride-2 view covers half of it)."""
         inp = self.inp
         hin = {"query": inp["query"].cpu().pin_memory(),
                "seq_lens": inp["seq_lens"].cpu().pin_memory(),
-               "table": inp["block_tables_storage"].cpu().pin_memory()}
+               "table": inp["block_tables"].cpu().contiguous().pin_memory()}
         if self.mode == "v2_splits":
             hin["cu"] = self.cu.cpu().pin_memory()
+        self._table_stage = (None if inp["block_tables"].is_contiguous() else
+                             torch.empty(hin["table"].shape, dtype=torch.int32,
+                                         device=inp["block_tables"].device))
         hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         return hin, hout
 
     def e2e_enqueue(self, hin, hout):
-        """H2D of the step's inputs, the step, D2H of its output (enqueued only)."""
+        """H2D of the step's inputs, the step, D2H of its output (enqueued only).
+        A strided table view is filled from a packed device copy."""
         inp = self.inp
         inp["query"].copy_(hin["query"], non_blocking=True)
         inp["seq_lens"].copy_(hin["seq_lens"], non_blocking=True)
-        inp["block_tables_storage"].copy_(hin["table"], non_blocking=True)
+        if self._table_stage is None:
+            inp["block_tables"].copy_(hin["table"], non_blocking=True)
+        else:
+            self._table_stage.copy_(hin["table"], non_blocking=True)
+            inp["block_tables"].copy_(self._table_stage)
         if "cu" in hin:
             self.cu.copy_(hin["cu"], non_blocking=True)
         self.run()
@@ -368,12 +411,14 @@ def oracle_sample_inputs(step_or_inp, seq_ids):
 def oracle_step(inp, spec, seq_ids, all_splits):
     """The oracle's pass over the sampled sequences (the same steps as the
     GPU step: metadata, then split-KV partition + reduce or single pass).
-    Returns (K/V bytes covered, seconds spent in the oracle itself); copying
-    the sampled pages out of device memory is not counted."""
+    Returns (K/V bytes covered, wall seconds spent in the oracle itself, process
+    CPU seconds over the same span, all threads); copying the sampled pages out
+    of device memory is not counted."""
     import oracle
 
     q, kc, vc, bt, lens = oracle_sample_inputs(inp, seq_ids)
     kw = oracle_variant_kwargs(inp)
+    c0 = time.process_time()
     t0 = time.perf_counter()
     if spec.mode == "v1":
         oracle.decode_v1(q, kc, vc, bt, lens, inp["scale"], **kw)
@@ -388,8 +433,9 @@ def oracle_step(inp, spec, seq_ids, all_splits):
                                           num_kv_splits=splits, **kw)
         oracle.v2_reduce(tmp, es, ml, lens, spec.block_size, num_kv_splits=splits)
     dt = time.perf_counter() - t0
+    dc = time.process_time() - c0
     e = inp["key_cache"].element_size()
-    return sum(lens) * spec.num_kv_heads * 2 * spec.head_size * e, dt
+    return sum(lens) * spec.num_kv_heads * 2 * spec.head_size * e, dt, dc
 
 
 def oracle_variant_kwargs(inp):
@@ -400,11 +446,13 @@ def oracle_variant_kwargs(inp):
                 alibi_slopes=None if sl is None else [float(v) for v in sl.cpu()])
 
 
-def cpu_threads():
-    try:
-        n = len(os.sched_getaffinity(0))
-    except Exception:
-        n = os.cpu_count() or 1
+def cpu_threads(n=None):
+    """Use ``n`` intra-op threads (default: every core this process may run on)."""
+    if n is None:
+        try:
+            n = len(os.sched_getaffinity(0))
+        except Exception:
+            n = os.cpu_count() or 1
     torch.set_num_threads(n)
     return torch.get_num_threads()
 
@@ -422,29 +470,39 @@ def oracle_metadata(inp, spec):
     return splits
 
 
-def cpu_baseline(inp, spec, budget_s=10.0):
+def cpu_baseline(inp, spec, budget_s=10.0, threads=None):
     """The oracle on a bounded sample: sequences in a seeded order until the
     oracle has spent the time budget (after one untimed warm-up sequence);
-    returns KV-read GB/s over the sample."""
-    cores = cpu_threads()
-    order = torch.randperm(len(inp["seq_lens_list"]), generator=torch.Generator().manual_seed(0))
-    order = order.tolist()
-    t0 = time.perf_counter()
-    splits = oracle_metadata(inp, spec)
-    spent = time.perf_counter() - t0
-    oracle_step(inp, spec, [order[-1]], splits)  # warm-up, not counted
-    done, nbytes = [], 0
-    for s in order:
-        nb, dt = oracle_step(inp, spec, [s], splits)
-        nbytes += nb
-        spent += dt
-        done.append(s)
-        if spent >= budget_s:
-            break
+    returns KV-read GB/s over the sample, the threads it was given and the
+    process CPU time over its wall time (how many cores it kept busy)."""
+    prev = torch.get_num_threads()
+    cores = cpu_threads(threads)
+    try:
+        order = torch.randperm(len(inp["seq_lens_list"]),
+                               generator=torch.Generator().manual_seed(0)).tolist()
+        c0 = time.process_time()
+        t0 = time.perf_counter()
+        splits = oracle_metadata(inp, spec)
+        spent = time.perf_counter() - t0
+        cpu = time.process_time() - c0
+        oracle_step(inp, spec, [order[-1]], splits)  # warm-up, not counted
+        done, nbytes = [], 0
+        for s in order:
+            nb, dt, dc = oracle_step(inp, spec, [s], splits)
+            nbytes += nb
+            spent += dt
+            cpu += dc
+            done.append(s)
+            if spent >= budget_s:
+                break
+    finally:
+        torch.set_num_threads(prev)
     return {"value": nbytes / spent / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "wall_s": round(spent, 3), "cpu_time_s": round(cpu, 3),
+            "cpu_time_over_wall": round(cpu / spent, 2),
             "sample": (f"{len(done)} of {len(inp['seq_lens_list'])} sequences "
                        f"({nbytes / 1e9:.3f} GB of K/V) of {spec.name} plus the whole batch's "
-                       f"metadata, float64, {spent:.1f} s of oracle time")}
+                       f"metadata, float64, {spent:.1f} s of oracle time on {cores} thread(s)")}
 
 
 # ------------------------------------------------------------------ arms --
@@ -468,34 +526,45 @@ def run_reference(args):
 
     def one_step():
         nonlocal pos
-        nb, n, spent = 0, 0, 0.0
+        nb, n, spent, cpu = 0, 0, 0.0, 0.0
         while True:
-            b, dt = oracle_step(inp, spec, [order[pos % len(order)]], splits)
+            b, dt, dc = oracle_step(inp, spec, [order[pos % len(order)]], splits)
             nb += b
             spent += dt
+            cpu += dc
             pos += 1
             n += 1
             if spent >= per_step:
                 break
-        return nb, spent, n
+        return nb, spent, cpu, n
 
     for _ in range(args.warmup):
         one_step()
-    tot_b, tot_t, tot_n = 0, 0.0, 0
+    tot_b, tot_t, tot_c, tot_n = 0, 0.0, 0.0, 0
     for _ in range(args.steps):
-        b, t, n = one_step()
+        b, t, c, n = one_step()
         tot_b += b
         tot_t += t
+        tot_c += c
         tot_n += n
     value = tot_b / tot_t / 1e9
+    cfg = workload_config(inp, world)
+    # one whole decode step of the workload at the sampled rate
+    ms_whole_step = cfg["kv_bytes_per_step"] / (value * 1e9) * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
+        "ms_per_step": round(ms_whole_step, 3),
+        "ms_per_step_note": ("one whole step of the workload extrapolated from the sampled "
+                             "rate: kv_bytes_per_step / value"),
+        "sample_ms_per_step": round(1e3 * tot_t / args.steps, 3),
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "description": spec.description},
+        "config": cfg,
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
-                         "kind": "oracle",
+                         "kind": "oracle", "wall_s": round(tot_t, 3),
+                         "cpu_time_s": round(tot_c, 3),
+                         "cpu_time_over_wall": round(tot_c / tot_t, 2),
                          "sample": (f"each step: sequences of {args.workload} in a seeded order "
                                     f"for ~{per_step:.1f} s ({tot_n} sequences over "
                                     f"{args.steps} steps), float64")},
@@ -504,6 +573,155 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# Workloads timed beside the headline in the same run, each with the same
+# steps and warm-up: the other decode configurations (single-pass MHA and GQA,
+# long-context split-KV, the tiny worked example) and the fp8-cache and ALiBi
+# variants of the hot path.
+COMPANION_WORKLOADS = ("mha_v1_fp16", "gqa_v1_bf16", "long_v2_bf16", "ragged_v2_fp8",
+                       "long_v2_fp8", "mha_v1_alibi_fp16", "tiny_mha_fp32")
+# Workloads whose oracle is also timed on one core (the small and mid-size
+# configurations); the headline's oracle runs on every core.
+ONE_CORE_WORKLOADS = ("tiny_mha_fp32", "mha_v1_fp16", "gqa_v1_bf16")
+
+ATTENTION_KERNEL = {"v1": "paged_attention_decode", "v2_fixed": "paged_attention_v2_partition",
+                    "v2_splits": "paged_attention_v2_partition"}
+
+
+def percentile(sorted_vals, q):
+    """Nearest-rank percentile of an ascending list (q in [0, 1])."""
+    i = min(len(sorted_vals) - 1, max(0, int(round(q * (len(sorted_vals) - 1)))))
+    return sorted_vals[i]
+
+
+def capture_step_graph(step):
+    """One step captured as a CUDA graph (after warm-up launches on a side stream)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step.run()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    return graph
+
+
+def time_steps(step, K, warmup, use_graph, dist=None, clocks=None):
+    """Device time of K steps, each bracketed by its own pair of CUDA events on
+    the launching stream.  Steps run back to back unless L2 is flushed between
+    them (the flush write is outside every pair).  Returns the per-step times
+    (ms), the whole span (ms), whether a graph was replayed and the clocks."""
+    flush = flushes_l2(step.inp)
+    flush_buf = (torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+                 if flush else None)
+    for _ in range(max(3, warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    graph = capture_step_graph(step) if use_graph else None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    for i in range(K):
+        if flush:
+            flush_buf.fill_(float(i))
+        ev[i][0].record()
+        if graph is not None:
+            graph.replay()
+        else:
+            step.run()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    per_step = [a.elapsed_time(b) for a, b in ev]
+    span = sum(per_step) if flush else ev[0][0].elapsed_time(ev[-1][1])
+    del flush_buf
+    return per_step, span, graph is not None, clk
+
+
+def kernel_breakdown(step, nsteps):
+    """Average device time of every launch of a step (events around each
+    launch, plain stream launches) and the attention kernel's launch times."""
+    kev = {}
+    for _ in range(nsteps):
+        step.run(kernel_events=kev)
+    torch.cuda.synchronize()
+    kernel_us = {k: round(sum(a.elapsed_time(b) for a, b in v) / len(v) * 1e3, 2)
+                 for k, v in kev.items()}
+    attn_ms = [a.elapsed_time(b) for a, b in kev[ATTENTION_KERNEL[step.mode]]]
+    return kernel_us, attn_ms
+
+
+def roofline_record(step, attn_ms, peak, peak_kind, workload):
+    attn_sorted = sorted(attn_ms)
+    avg_ms = sum(attn_ms) / len(attn_ms)
+    achieved = step.attn_alg_bytes / (avg_ms * 1e-3) / 1e9
+    return {
+        "kernel": ATTENTION_KERNEL[step.mode],
+        "bound": "hbm",
+        "achieved": round(achieved, 1),
+        "peak": peak,
+        "peak_kind": f"{peak_kind} HBM copy bandwidth",
+        "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "traffic": recorded_traffic(workload),
+        "alg_bytes_per_launch": step.attn_alg_bytes,
+        "avg_launch_us": round(avg_ms * 1e3, 2),
+        "p10_p90_launch_us": [round(percentile(attn_sorted, 0.1) * 1e3, 2),
+                              round(percentile(attn_sorted, 0.9) * 1e3, 2)],
+    }
+
+
+def step_stats(per_step_ms):
+    v = sorted(per_step_ms)
+    return {"median": round(percentile(v, 0.5) * 1e3, 2), "p10": round(percentile(v, 0.1) * 1e3, 2),
+            "p90": round(percentile(v, 0.9) * 1e3, 2)}
+
+
+def dtype_label(spec):
+    return spec.dtype if spec.kv_cache_dtype == "auto" else f"{spec.dtype}+{spec.kv_cache_dtype}"
+
+
+def companion_record(name, args, peak, peak_kind, want_one_core):
+    """Time one companion workload (same steps and warm-up as the headline)
+    and, for the small and mid-size configurations, its oracle on one core."""
+    step = DecodeStep(name, seed=0, device="cuda")
+    K = args.steps
+    clocks = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+    per_step, span, graphed, clk = time_steps(step, K, args.warmup, args.graph, clocks=clocks)
+    kernel_us, attn_ms = kernel_breakdown(step, min(K, 200))
+    ms = span / K
+    rec = {
+        "us_per_step": round(ms * 1e3, 2),
+        "step_us": step_stats(per_step),
+        "value": round(step.kv_bytes / (ms * 1e-3) / 1e9, 2),
+        "unit": UNIT,
+        "dtype": dtype_label(step.spec),
+        "config": step.config(),
+        "roofline": roofline_record(step, attn_ms, peak, peak_kind, name),
+        "kernel_us": kernel_us,
+        "gpu_launches": K * step.launches_per_step,
+        "launch": "CUDA graph replay of the step" if graphed else "stream launches",
+        "clocks": clk,
+    }
+    if want_one_core:
+        rec["cpu_baseline_1core"] = cpu_baseline(step.inp, step.spec, budget_s=args.one_core_budget,
+                                                 threads=1)
+    del step
+    torch.cuda.empty_cache()
+    return rec
 
 
 def run_ours(args):
@@ -529,83 +747,13 @@ def run_ours(args):
     if args.warps:
         step.pkv.set_attention_warps(args.warps)
     spec = step.spec
-    flush = step.kv_bytes < 4 * L2_BYTES
-    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda") if flush else None
-
-    for _ in range(max(3, args.warmup)):
-        step.run()
-    torch.cuda.synchronize()
-
     K = args.steps
-    graph = None
-    if args.graph:
-        # one step captured as a CUDA graph and replayed (no per-launch events
-        # inside it; the attention kernel is then timed by the per-kernel pass)
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            for _ in range(3):
-                step.run()
-        torch.cuda.current_stream().wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step.run()
-        for _ in range(3):
-            graph.replay()
-        torch.cuda.synchronize()
-    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
     clocks = ClockSampler(torch.cuda.current_device()) if (rank == 0 and not args.no_clocks) else None
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    if clocks:
-        clocks.start()
-        time.sleep(0.3)
-    if flush:
-        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(K)]
-        for i in range(K):
-            flush_buf.fill_(float(i))
-            step_ev[i][0].record()
-            if graph is not None:
-                graph.replay()
-            else:
-                step.run(attn_ev[i])
-            step_ev[i][1].record()
-        torch.cuda.synchronize()
-        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
-    else:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record()
-        if graph is not None:
-            for i in range(K):
-                graph.replay()
-        else:
-            for i in range(K):
-                step.run(attn_ev[i])
-        t_end.record()
-        torch.cuda.synchronize()
-        elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        dist.barrier()
-    clk = clocks.stop() if clocks else None
-    attn_ms = None if graph is not None else [a.elapsed_time(b) for a, b in attn_ev]
-
-    elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
+    per_step, span_ms, graphed, clk = time_steps(step, K, args.warmup, args.graph, dist, clocks)
+    elapsed_ms = max_over_ranks(span_ms, dist, "cuda")
 
     # per-kernel breakdown over a separate run of steps (events around every launch)
-    kev = {}
-    nb = min(K, 200)
-    for _ in range(nb):
-        step.run(kernel_events=kev)
-    torch.cuda.synchronize()
-    kernel_us = {k: round(sum(a.elapsed_time(b) for a, b in v) / len(v) * 1e3, 2)
-                 for k, v in kev.items()}
-    if attn_ms is None:
-        attn_key = "paged_attention_decode" if step.mode == "v1" else "paged_attention_v2_partition"
-        attn_ms = [a.elapsed_time(b) for a, b in kev[attn_key]]
+    kernel_us, attn_ms = kernel_breakdown(step, min(K, 200))
 
     # end to end through host buffers (per step: H2D of the inputs, the step,
     # D2H of the output, host waits for it)
@@ -639,16 +787,11 @@ def run_ours(args):
 
     ms_step = elapsed_ms / K
     value = aggregate_gbs(step.kv_bytes, world, ms_step * 1e-3)
-    attn_sorted = sorted(attn_ms)
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
     peak, peak_kind = load_peak()
-    achieved = step.attn_alg_bytes / (attn_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    roofline = roofline_record(step, attn_ms, peak, peak_kind, args.workload)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(step.inp, spec, budget_s=args.cpu_budget)
-    kern = {"v1": "paged_attention_decode", "v2_fixed": "paged_attention_v2_partition",
-            "v2_splits": "paged_attention_v2_partition"}[step.mode]
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -658,54 +801,47 @@ def run_ours(args):
         "warmup": max(3, args.warmup),
         "ms_per_step": round(ms_step, 5),
         "us_per_step": round(ms_step * 1e3, 2),
+        "step_us": step_stats(per_step),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": spec.dtype if spec.kv_cache_dtype == "auto" else f"{spec.dtype}+{spec.kv_cache_dtype}",
+        "dtype": dtype_label(spec),
         "accumulate": "f32",
         "data": "synthetic (seeded; see workloads.py)",
-        "config": {
-            "workload": args.workload,
-            "description": spec.description,
-            "num_seqs": step.B, "num_heads": step.H, "num_kv_heads": step.Hk,
-            "head_size": step.D, "block_size": step.bs,
-            "kv_cache_dtype": spec.kv_cache_dtype, "alibi": spec.alibi,
-            "total_tokens": sum(step.lens), "kv_bytes_per_step": step.kv_bytes,
-            "l2": ("flushed between steps (512 MB write)" if flush else
-                   f"inputs larger than L2: {step.kv_bytes / 1e9:.2f} GB of K/V per step"),
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "launch": ("CUDA graph replay of the step" if graph is not None else
-                       "stream launches, programmatic dependent launch"),
-            "metadata": ("one launch (prepare_decode_metadata)" if step.fused_metadata else
-                         "copy_page_indices + compute_num_kv_splits") if step.mode == "v2_splits" else None,
-        },
-        "roofline": {
-            "kernel": kern,
-            "bound": "hbm",
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "peak_kind": f"{peak_kind} HBM copy bandwidth",
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "traffic": traffic,
-            "alg_bytes_per_launch": step.attn_alg_bytes,
-            "avg_launch_us": round(attn_avg_ms * 1e3, 2),
-            "p10_p90_launch_us": [round(attn_sorted[len(attn_sorted) // 10] * 1e3, 2),
-                                  round(attn_sorted[(9 * len(attn_sorted)) // 10] * 1e3, 2)],
-        },
-        "step_share": {"attention_kernel": round(attn_avg_ms / ms_step, 4)},
+        "config": step.config(world),
+        "launch": ("CUDA graph replay of the step" if graphed else
+                   "stream launches, programmatic dependent launch"),
+        "metadata": (("one launch (prepare_decode_metadata)" if step.fused_metadata else
+                      "copy_page_indices + compute_num_kv_splits")
+                     if step.mode == "v2_splits" else None),
+        "roofline": roofline,
+        "step_share": {"attention_kernel": round(roofline["avg_launch_us"] / 1e3 / ms_step, 4)},
         "kernel_us": kernel_us,
         "e2e": {"value": round(aggregate_gbs(step.kv_bytes, world, e2e_s / Ke), 2), "unit": UNIT,
                 "us_per_step": round(e2e_s / Ke * 1e6, 2), "steps": Ke,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": ("K/V cache resident on the device; per step: H2D of the inputs from "
-                         "pinned host memory, the step, D2H of the output, host waits"
+                "note": ("K/V cache resident on the device; per step: H2D of the inputs (the "
+                         "table as its packed live view) from pinned host memory, the step, D2H "
+                         "of the output, host waits"
                          + ("; replayed as one CUDA graph" if e2e_graph is not None else "")),
                 "graph": e2e_graph is not None},
         "gpu_launches": K * step.launches_per_step,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    if world == 1 and not args.no_companions and args.num_seqs is None:
+        # the other configurations, one after another with the same steps and
+        # warm-up; the headline's buffers are released first
+        del step, hin, hout, e2e_graph
+        torch.cuda.empty_cache()
+        comp = {}
+        for name in COMPANION_WORKLOADS:
+            if name == args.workload:
+                continue
+            comp[name] = companion_record(name, args, peak, peak_kind,
+                                          (not args.no_cpu_baseline) and name in ONE_CORE_WORKLOADS)
+        line["workloads"] = comp
+        line["gpu_launches"] += sum(r["gpu_launches"] for r in comp.values())
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -911,6 +1047,10 @@ def main(argv=None):
                     help="seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--reference-budget", type=float, default=120.0,
                     help="total seconds of oracle work for --impl reference (all steps)")
+    ap.add_argument("--one-core-budget", type=float, default=3.0,
+                    help="seconds of single-thread oracle work per small/mid-size workload")
+    ap.add_argument("--no-companions", action="store_true",
+                    help="time only the selected workload (no per-configuration records)")
     args = ap.parse_args(argv)
     if args.workload in workloads.SWA_SPEC_WORKLOADS:
         if args.impl == "reference":

@@ -148,12 +148,14 @@ const char *pkv_status_string(pkv_status_t status);
 size_t pkv_decode_args_size(void);
 
 /*
- * Tuning knob for paged_attention_decode / paged_attention_v2_partition: warps
- * per CTA, i.e. how many warps split one (sequence, kv head, partition) unit.
- * 0 (default) picks per call from the pass (single or split), the number of
- * units and the SM count (see the launcher for the measured rule);
- * 1, 2 or 4 forces that value where the instance exists.  Process-wide.
- * Returns PKV_ERR_INVALID_ARG for any other value.
+ * Tuning override for benchmarks and tests, not for serving: warps per CTA of
+ * paged_attention_decode / paged_attention_v2_partition, i.e. how many warps
+ * split one (sequence, kv head, partition) unit.  0 (default) lets every call
+ * pick from its own pass (single or split), number of units and SM count (the
+ * measured rule in the launcher); 1, 2 or 4 forces that value, where the
+ * instance exists, on every later call of every thread until it is set back
+ * to 0.  A serving process leaves it at 0.  Returns PKV_ERR_INVALID_ARG for
+ * any other value.
  */
 pkv_status_t pkv_set_attention_warps(int32_t warps);
 
@@ -167,10 +169,12 @@ pkv_status_t pkv_set_attention_warps(int32_t warps);
 pkv_status_t pkv_set_wait_limit_ns(uint64_t ns);
 
 /*
- * Test hook for the timeout path above: every stage of the attention kernels
- * then expects `bytes` (a multiple of 16, at most 65536) more than its copies
- * deliver, so each of its waits runs into the limit.  0 (default) turns it
- * off.  Only for exercising failure detection; process-wide.
+ * Test hook for the timeout path above, one-shot: every stage of the NEXT
+ * attention launch (paged_attention_decode or paged_attention_v2_partition, in
+ * any thread) expects `bytes` (a multiple of 16, at most 65536) more than its
+ * copies deliver, so each of its waits runs into the limit.  That launch
+ * clears the hook; later launches are unaffected.  0 clears it without a
+ * launch.  Only for exercising failure detection.
  */
 pkv_status_t pkv_test_set_unarrived_bytes(uint32_t bytes);
 
@@ -420,9 +424,16 @@ size_t pkv_swa_spec_args_size(void);
  *   max_num_partitions, partition_size, num_kv_splits, args: as for
  *       paged_attention_v2_partition.
  *
+ * Arguments are checked exactly as paged_attention_v2_partition checks them
+ * (PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED) before the scratch size is; the
+ * size check cannot overflow, whatever the head and partition counts.
+ *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array and it
+ * (cudaGetSymbolAddress, with that device current) and caches it for the life
+ * of the process; make that first call before any stream capture.  A
+ * cudaDeviceReset reloads the library's module and leaves that cached address
+ * stale: a process that resets a device must not call this entry point
+ * afterwards.  All calls share the one array and it
  * keeps the last call's contents (every value a call reads is written by the
  * same call first): calls that overlap on the GPU, on different streams,
  * race on it.

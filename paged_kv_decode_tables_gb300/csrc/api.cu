@@ -143,7 +143,9 @@ AttnParams make_params(const pkv_decode_args_t *a) {
   p.out_scale = fp8 ? a->v_scale : 1.0f;
   p.alibi = a->alibi_slopes;
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-  p.extra_expect_tx = g_extra_expect_tx.load(std::memory_order_relaxed);
+  // The test hook is one-shot: the launch that reads it clears it, so a hook
+  // left set can delay at most one launch, never every later one.
+  p.extra_expect_tx = g_extra_expect_tx.exchange(0u, std::memory_order_relaxed);
   return p;
 }
 
@@ -235,18 +237,10 @@ pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float
                                           int32_t max_num_partitions, int32_t partition_size,
                                           const int32_t *num_kv_splits,
                                           const pkv_decode_args_t *args, pkv_stream_t stream) {
-  pkv_status_t st = check_decode_args(args);
+  pkv_status_t st = pkv::check_partition_args(args, max_num_partitions, partition_size,
+                                              num_kv_splits);
   if (st != PKV_OK) return st;
   if (!tmp_out || !exp_sums || !max_logits) return PKV_ERR_INVALID_ARG;
-  if (max_num_partitions < 1) return PKV_ERR_INVALID_ARG;
-  if (num_kv_splits == nullptr) {
-    if (partition_size < args->block_size || partition_size % args->block_size != 0)
-      return PKV_ERR_INVALID_ARG;
-    const int64_t need =
-        (int64_t(args->max_blocks_per_seq) * args->block_size + partition_size - 1) /
-        partition_size;
-    if (args->kv_indptr == nullptr && need > max_num_partitions) return PKV_ERR_INVALID_ARG;
-  }
   if (args->num_seqs == 0) return PKV_OK;
   AttnParams p = make_params(args);
   p.mode = num_kv_splits ? pkv::kModeSplits : pkv::kModeFixed;
@@ -351,6 +345,22 @@ pkv_status_t prepare_decode_metadata(int32_t *page_indices, int64_t page_indices
 }  // extern "C"
 
 namespace pkv {
+
+pkv_status_t check_partition_args(const pkv_decode_args_t *args, int32_t max_num_partitions,
+                                  int32_t partition_size, const int32_t *num_kv_splits) {
+  pkv_status_t st = check_decode_args(args);
+  if (st != PKV_OK) return st;
+  if (max_num_partitions < 1) return PKV_ERR_INVALID_ARG;
+  if (num_kv_splits == nullptr) {
+    if (partition_size < args->block_size || partition_size % args->block_size != 0)
+      return PKV_ERR_INVALID_ARG;
+    const int64_t need =
+        (int64_t(args->max_blocks_per_seq) * args->block_size + partition_size - 1) /
+        partition_size;
+    if (args->kv_indptr == nullptr && need > max_num_partitions) return PKV_ERR_INVALID_ARG;
+  }
+  return PKV_OK;
+}
 
 pkv_status_t launch_attention(pkv_dtype_t dtype, pkv_kv_cache_dtype_t kv, const AttnParams &p,
                               int head_size, int block_size, int warps, dim3 grid,

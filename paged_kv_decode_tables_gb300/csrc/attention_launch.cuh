@@ -18,6 +18,11 @@ pkv_status_t launch_attention(pkv_dtype_t dtype, pkv_kv_cache_dtype_t kv, const 
                               int head_size, int block_size, int warps, dim3 grid,
                               cudaStream_t stream);
 
+// The host-side argument checks of paged_attention_v2_partition (everything
+// but its three scratch pointers), shared with the entry points built on it.
+pkv_status_t check_partition_args(const pkv_decode_args_t *args, int32_t max_num_partitions,
+                                  int32_t partition_size, const int32_t *num_kv_splits);
+
 namespace detail {
 
 // Opt every launched instance into its dynamic shared memory size, once per

@@ -15,6 +15,7 @@
 #include <cstdint>
 
 #include "../../include/paged_kv.h"
+#include "attention_launch.cuh"
 
 static constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB per GPU
 
@@ -31,7 +32,9 @@ size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Device address of the array on the current device.  Host code only sees a
 // host-side stand-in under the array's name, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached for the life of the
+// process: a cudaDeviceReset reloads the module and leaves the cached address
+// stale, so the entry point is not for processes that reset a device.
 void *scratch_address(int dev) {
   void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
   if (p != nullptr) return p;
@@ -39,6 +42,27 @@ void *scratch_address(int dev) {
   if (cudaGetSymbolAddress(&q, g_split_scratch) != cudaSuccess || q == nullptr) return nullptr;
   g_scratch_addr[dev].store(q, std::memory_order_release);
   return q;
+}
+
+// Bytes of the three scratch regions (tmp_out, exp_sums, max_logits, each
+// rounded up to kAlign) for `rows` = num_seqs * num_heads * max_num_partitions
+// rows of head_size floats; false when they exceed the array.  Every product
+// is bounded by a division first, so no size computation can wrap whatever
+// the (already validated, positive) factors are.
+bool scratch_layout(int64_t num_seqs, int64_t num_heads, int64_t max_parts, int64_t head_size,
+                    size_t *tmp_bytes, size_t *stat_bytes) {
+  const uint64_t row_bytes = (uint64_t(head_size) + 2u) * sizeof(float);
+  const uint64_t max_rows = kScratchBytes / row_bytes;
+  uint64_t rows = uint64_t(num_seqs);
+  if (rows > max_rows) return false;
+  if (uint64_t(num_heads) > max_rows / rows) return false;
+  rows *= uint64_t(num_heads);
+  if (uint64_t(max_parts) > max_rows / rows) return false;
+  rows *= uint64_t(max_parts);
+  // rows * row_bytes <= kScratchBytes here, so nothing below wraps.
+  *tmp_bytes = round_up(size_t(rows) * size_t(head_size) * sizeof(float));
+  *stat_bytes = round_up(size_t(rows) * sizeof(float));
+  return *tmp_bytes + 2 * *stat_bytes <= kScratchBytes;
 }
 
 }  // namespace
@@ -51,14 +75,17 @@ extern "C" pkv_status_t paged_attention_v2_noalloc(void *out, const int64_t out_
                                                    const int32_t *num_kv_splits,
                                                    const pkv_decode_args_t *args,
                                                    pkv_stream_t stream) {
-  if (args == nullptr || out == nullptr || out_stride == nullptr) return PKV_ERR_INVALID_ARG;
-  if (args->num_seqs < 0 || args->num_heads < 1 || args->head_size < 1 || max_num_partitions < 1)
-    return PKV_ERR_INVALID_ARG;
+  // The partition pass's own checks come first, so a malformed call gets the
+  // status that names its fault rather than a scratch-size refusal.
+  pkv_status_t st =
+      pkv::check_partition_args(args, max_num_partitions, partition_size, num_kv_splits);
+  if (st != PKV_OK) return st;
+  if (out == nullptr || out_stride == nullptr) return PKV_ERR_INVALID_ARG;
   if (args->num_seqs == 0) return PKV_OK;
-  const size_t rows = size_t(args->num_seqs) * size_t(args->num_heads) * size_t(max_num_partitions);
-  const size_t tmp_bytes = round_up(rows * size_t(args->head_size) * sizeof(float));
-  const size_t stat_bytes = round_up(rows * sizeof(float));
-  if (tmp_bytes + 2 * stat_bytes > kScratchBytes) return PKV_ERR_SCRATCH_TOO_SMALL;
+  size_t tmp_bytes = 0, stat_bytes = 0;
+  if (!scratch_layout(args->num_seqs, args->num_heads, max_num_partitions, args->head_size,
+                      &tmp_bytes, &stat_bytes))
+    return PKV_ERR_SCRATCH_TOO_SMALL;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
   unsigned char *base = static_cast<unsigned char *>(scratch_address(dev));
@@ -68,8 +95,8 @@ extern "C" pkv_status_t paged_attention_v2_noalloc(void *out, const int64_t out_
   float *max_logits = reinterpret_cast<float *>(base + tmp_bytes + stat_bytes);
   // Every entry the reduce reads is written by the partition pass first, so
   // nothing left from an earlier call needs clearing.
-  pkv_status_t st = paged_attention_v2_partition(tmp, exp_sums, max_logits, max_num_partitions,
-                                                 partition_size, num_kv_splits, args, stream);
+  st = paged_attention_v2_partition(tmp, exp_sums, max_logits, max_num_partitions,
+                                    partition_size, num_kv_splits, args, stream);
   if (st != PKV_OK) return st;
   return paged_attention_v2_reduce(out, out_stride, tmp, exp_sums, max_logits, args->seq_lens,
                                    num_kv_splits, args->num_seqs, args->num_heads,

@@ -162,6 +162,45 @@ def test_partition_rejects_bad_partitioning(lib):
     assert lib.paged_attention_v2_partition(p, p, p, 0, 16, None, ctypes.byref(a), None) == 1
 
 
+def test_noalloc_scratch_bound_cannot_overflow(lib):
+    """The no-allocation entry point refuses a request beyond its fixed array
+    before enqueuing anything, however large the head and partition counts:
+    32768 seqs x 2^17 heads x 2^30 partitions is 2^62 rows, whose byte count
+    wraps to 0 in 64-bit arithmetic."""
+    out, s = 0x3000, (ctypes.c_int64 * 3)(1, 1, 1)
+    splits = 0x5000  # split counts given: no partition-size rule applies
+    a = _args(num_seqs=1 << 15, num_heads=1 << 17, num_kv_heads=1 << 14)
+    st = lib.paged_attention_v2_noalloc(out, s, 1 << 30, 0, splits, ctypes.byref(a), None)
+    assert st == 4  # PKV_ERR_SCRATCH_TOO_SMALL
+    # each factor alone beyond the array
+    for kw, parts in (({"num_seqs": 65535}, 1024), ({"num_heads": 65535 * 8, "num_kv_heads": 65535},
+                                                    1), ({}, (1 << 31) - 1)):
+        st = lib.paged_attention_v2_noalloc(out, s, parts, 0, splits, ctypes.byref(_args(**kw)),
+                                            None)
+        assert st == 4, kw
+
+
+def test_noalloc_checks_arguments_before_its_scratch_size(lib):
+    """A malformed call gets the partition pass's own status (not a
+    scratch-size refusal), even when its sizes would also overflow the array."""
+    out, s, splits = 0x3000, (ctypes.c_int64 * 3)(1, 1, 1), 0x5000
+    huge = 1 << 30
+    assert lib.paged_attention_v2_noalloc(out, s, huge, 0, splits,
+                                          ctypes.byref(_args(head_size=96)), None) == 2
+    assert lib.paged_attention_v2_noalloc(out, s, huge, 0, splits,
+                                          ctypes.byref(_args(num_seqs=70000)), None) == 2
+    assert lib.paged_attention_v2_noalloc(out, s, huge, 0, splits,
+                                          ctypes.byref(_args(query=None)), None) == 1
+    # fixed partitions: partition size not a multiple of block_size
+    assert lib.paged_attention_v2_noalloc(out, s, huge, 24, None, ctypes.byref(_args()),
+                                          None) == 1
+    assert lib.paged_attention_v2_noalloc(out, s, 0, 0, splits, ctypes.byref(_args()), None) == 1
+    assert lib.paged_attention_v2_noalloc(0, s, 4, 0, splits, ctypes.byref(_args()), None) == 1
+    # an empty batch is a no-op, whatever it would need
+    assert lib.paged_attention_v2_noalloc(out, s, huge, 0, splits,
+                                          ctypes.byref(_args(num_seqs=0)), None) == 0
+
+
 def test_reduce_and_metadata_reject_bad_arguments(lib):
     s = (ctypes.c_int64 * 3)(1, 1, 1)
     p = 0x4000

@@ -23,6 +23,15 @@ def test_reference_arm_json_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["unit"] == line["unit"]
     assert line["config"]["workload"] == "tiny_mha_fp32"
+    # the same configuration dict the library arm emits for this workload
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    assert line["config"] == bench.workload_config(workloads.make_workload("tiny_mha_fp32", seed=0))
+    # ms_per_step is one whole step at the sampled rate
+    kvb = line["config"]["kv_bytes_per_step"]
+    assert abs(line["ms_per_step"] - kvb / (line["value"] * 1e9) * 1e3) <= 1e-3 * line["ms_per_step"] + 2e-3
+    assert line["cpu_baseline"]["cpu_time_s"] >= 0 and "cpu_time_over_wall" in line["cpu_baseline"]
 
 
 def test_reference_arm_declines_library_only_workloads():
@@ -47,8 +56,34 @@ def test_oracle_step_covers_fp8_and_alibi_workloads():
         assert kw["kv_cache_dtype"] == spec.kv_cache_dtype
         assert (kw["alibi_slopes"] is not None) == spec.alibi
         splits = bench.oracle_metadata(inp, spec)
-        nbytes, seconds = bench.oracle_step(inp, spec, [0, 2], splits)
+        nbytes, seconds, cpu_seconds = bench.oracle_step(inp, spec, [0, 2], splits)
         e = 1 if spec.kv_cache_dtype != "auto" else 2
         lens = inp["seq_lens_list"]
         assert nbytes == (lens[0] + lens[2]) * spec.num_kv_heads * 2 * spec.head_size * e
-        assert seconds > 0
+        assert seconds > 0 and cpu_seconds >= 0
+
+
+def test_cpu_baseline_reports_threads_and_cpu_time():
+    """The CPU leg states the threads it gave the oracle and measures how busy
+    it kept them (process CPU time over wall time)."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    inp = workloads.make_workload("tiny_mha_fp32", seed=0)
+    before = torch.get_num_threads()
+    rec = bench.cpu_baseline(inp, inp["spec"], budget_s=0.2, threads=1)
+    assert rec["cores"] == 1 and rec["kind"] == "oracle" and rec["value"] > 0
+    assert rec["wall_s"] > 0 and rec["cpu_time_s"] >= 0
+    assert abs(rec["cpu_time_over_wall"] - rec["cpu_time_s"] / rec["wall_s"]) <= 0.02 + 0.01 * rec["cpu_time_over_wall"]
+    assert torch.get_num_threads() == before  # the thread count is restored
+
+
+def test_step_statistics():
+    sys.path.insert(0, ROOT)
+    import bench
+    ms = [0.5 + 0.01 * i for i in range(20)]
+    st = bench.step_stats(list(reversed(ms)))
+    assert st["p10"] <= st["median"] <= st["p90"]
+    assert st["median"] == round(bench.percentile(sorted(ms), 0.5) * 1e3, 2)
+    assert bench.percentile([1.0], 0.9) == 1.0
