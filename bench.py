@@ -613,10 +613,13 @@ def capture_step_graph(step):
 
 
 def time_steps(step, K, warmup, use_graph, dist=None, clocks=None):
-    """Device time of K steps, each bracketed by its own pair of CUDA events on
-    the launching stream.  Steps run back to back unless L2 is flushed between
-    them (the flush write is outside every pair).  Returns the per-step times
-    (ms), the whole span (ms), whether a graph was replayed and the clocks."""
+    """Device time of K steps on the launching stream.  Inputs larger than L2:
+    the K steps run back to back between two CUDA events (the timed span),
+    then a second run of K steps, each bracketed by its own pair of events,
+    gives the per-step distribution.  Smaller inputs: L2 is flushed before
+    every step (outside its pair of events) and the span is the sum of the
+    per-step times.  Returns the per-step times (ms), the span (ms), whether a
+    graph was replayed and the clocks sampled during the timed span."""
     flush = flushes_l2(step.inp)
     flush_buf = (torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
                  if flush else None)
@@ -624,6 +627,13 @@ def time_steps(step, K, warmup, use_graph, dist=None, clocks=None):
         step.run()
     torch.cuda.synchronize()
     graph = capture_step_graph(step) if use_graph else None
+
+    def one():
+        if graph is not None:
+            graph.replay()
+        else:
+            step.run()
+
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     if dist is not None:
@@ -632,21 +642,33 @@ def time_steps(step, K, warmup, use_graph, dist=None, clocks=None):
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    for i in range(K):
-        if flush:
+    if flush:
+        for i in range(K):
             flush_buf.fill_(float(i))
-        ev[i][0].record()
-        if graph is not None:
-            graph.replay()
-        else:
-            step.run()
-        ev[i][1].record()
+            ev[i][0].record()
+            one()
+            ev[i][1].record()
+    else:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(K):
+            one()
+        t1.record()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    per_step = [a.elapsed_time(b) for a, b in ev]
-    span = sum(per_step) if flush else ev[0][0].elapsed_time(ev[-1][1])
+    if flush:
+        per_step = [a.elapsed_time(b) for a, b in ev]
+        span = sum(per_step)
+    else:
+        span = t0.elapsed_time(t1)
+        for i in range(K):
+            ev[i][0].record()
+            one()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        per_step = [a.elapsed_time(b) for a, b in ev]
     del flush_buf
     return per_step, span, graph is not None, clk
 
@@ -746,6 +768,8 @@ def run_ours(args):
                       fused_metadata=args.metadata == "fused")
     if args.warps:
         step.pkv.set_attention_warps(args.warps)
+    if args.fp8_kernel == "tensor-memory":
+        step.pkv.set_fp8_kernel(1)
     spec = step.spec
     K = args.steps
     clocks = ClockSampler(torch.cuda.current_device()) if (rank == 0 and not args.no_clocks) else None
@@ -811,6 +835,7 @@ def run_ours(args):
         "config": step.config(world),
         "launch": ("CUDA graph replay of the step" if graphed else
                    "stream launches, programmatic dependent launch"),
+        "fp8_kernel": args.fp8_kernel if spec.kv_cache_dtype != "auto" else None,
         "metadata": (("one launch (prepare_decode_metadata)" if step.fused_metadata else
                       "copy_page_indices + compute_num_kv_splits")
                      if step.mode == "v2_splits" else None),
@@ -1037,6 +1062,8 @@ def main(argv=None):
                     help="smaller batch of the same workload (profiling captures only)")
     ap.add_argument("--warps", type=int, default=0, choices=[0, 1, 2, 4],
                     help="force warps per attention CTA (0: library default)")
+    ap.add_argument("--fp8-kernel", choices=["mma", "tensor-memory"], default="mma",
+                    help="kernel for fp8 caches of head size 128 / block size 16")
     ap.add_argument("--metadata", choices=["fused", "separate"], default="fused",
                     help="ragged step: metadata in one launch or the two separate kernels")
     ap.add_argument("--no-graph", dest="graph", action="store_false",

@@ -160,6 +160,23 @@ size_t pkv_decode_args_size(void);
 pkv_status_t pkv_set_attention_warps(int32_t warps);
 
 /*
+ * Kernel for fp8 caches (kv_cache_dtype E4M3 / E5M2) with head_size 128,
+ * block_size 16 and fp16/bf16 queries, process-wide:
+ *   0 (default): the mma.sync kernel (codes widened to f16 in registers);
+ *   1: the tensor-memory kernel: persistent CTAs that take unstarted CTAs'
+ *      work from the launch queue (cluster launch control), both products as
+ *      tcgen05 kind::f8f6f4 MMAs on the cache codes in shared memory, the
+ *      query as an exact sum of E4M3 terms, probabilities as four E4M3 terms
+ *      (about 16 significant bits), accumulators in tensor memory.  Same
+ *      results within the tolerances of the mma.sync kernel; slower on the
+ *      measured batches.  A forced warp count (pkv_set_attention_warps)
+ *      selects the mma.sync kernel.
+ * Other shapes always use the mma.sync kernel.  Returns PKV_ERR_INVALID_ARG
+ * for any other value.
+ */
+pkv_status_t pkv_set_fp8_kernel(int32_t which);
+
+/*
  * Limit, in nanoseconds, of every wait of the attention kernels for a stage's
  * copies into shared memory (default 2 s; 0 restores it; at most 60 s).  A
  * wait that runs out sets PKV_ERRF_TIMEOUT, waits (again bounded) for the

@@ -25,6 +25,7 @@ __all__ = [
     "version",
     "set_attention_warps",
     "set_wait_limit_ns",
+    "set_fp8_kernel",
     "paged_attention_decode",
     "paged_attention_v2_partition",
     "paged_attention_v2_reduce",
@@ -133,6 +134,8 @@ def lib() -> ctypes.CDLL:
     L.pkv_decode_args_size.argtypes = []
     L.pkv_set_attention_warps.restype = ctypes.c_int
     L.pkv_set_attention_warps.argtypes = [_c_i32]
+    L.pkv_set_fp8_kernel.restype = ctypes.c_int
+    L.pkv_set_fp8_kernel.argtypes = [_c_i32]
     L.pkv_set_wait_limit_ns.restype = ctypes.c_int
     L.pkv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.pkv_test_set_unarrived_bytes.restype = ctypes.c_int
@@ -211,6 +214,12 @@ def set_attention_warps(warps: int) -> None:
     """Force warps per CTA (1, 2 or 4) for the attention kernels where that
     instance exists; 0 restores the measured per-call choice."""
     _check(lib().pkv_set_attention_warps(int(warps)), "pkv_set_attention_warps")
+
+
+def set_fp8_kernel(which: int) -> None:
+    """Kernel for fp8 caches (head size 128, block size 16): 0 the mma.sync
+    kernel (default), 1 the tensor-memory kernel (see ``pkv_set_fp8_kernel``)."""
+    _check(lib().pkv_set_fp8_kernel(int(which)), "pkv_set_fp8_kernel")
 
 
 def set_wait_limit_ns(ns: int) -> None:

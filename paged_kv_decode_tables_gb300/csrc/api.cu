@@ -20,6 +20,7 @@ std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_forced_warps{0};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<unsigned> g_extra_expect_tx{0};
+std::atomic<int> g_fp8_kernel{0};
 
 int sm_count() {
   int dev = 0;
@@ -175,6 +176,14 @@ int pick_warps(const pkv_decode_args_t *a, int64_t units, Pass pass, int partiti
   return want;
 }
 
+// fp8 caches of head size 128 / block size 16 run on the tensor-memory kernel
+// when it is selected (pkv_set_fp8_kernel(1)) and no warp count is forced (a
+// forced count names instances of the mma.sync kernel).
+bool use_tensor_memory_kernel(const pkv_decode_args_t *a) {
+  return g_fp8_kernel.load(std::memory_order_relaxed) == 1 &&
+         g_forced_warps.load(std::memory_order_relaxed) == 0 && pkv::fp8_tc_eligible(a);
+}
+
 }  // namespace
 
 extern "C" {
@@ -197,6 +206,12 @@ size_t pkv_decode_args_size(void) { return sizeof(pkv_decode_args_t); }
 pkv_status_t pkv_set_attention_warps(int32_t warps) {
   if (warps != 0 && warps != 1 && warps != 2 && warps != 4) return PKV_ERR_INVALID_ARG;
   g_forced_warps.store(warps, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+pkv_status_t pkv_set_fp8_kernel(int32_t which) {
+  if (which != 0 && which != 1) return PKV_ERR_INVALID_ARG;
+  g_fp8_kernel.store(which, std::memory_order_relaxed);
   return PKV_OK;
 }
 
@@ -227,6 +242,8 @@ pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
   p.o_s2 = out_stride[2];
   p.max_parts = 1;
   dim3 grid(1, args->num_kv_heads * p.head_groups, args->num_seqs);
+  if (use_tensor_memory_kernel(args))
+    return pkv::launch_attention_fp8_tc(args, p, grid, reinterpret_cast<cudaStream_t>(stream));
   const int w = pick_warps(args, int64_t(grid.y) * args->num_seqs, Pass::kSingle, 0);
   return pkv::launch_attention(args->dtype, pkv_kv_cache_dtype_t(args->kv_cache_dtype), p,
                                args->head_size, args->block_size, w, grid,
@@ -251,6 +268,8 @@ pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float
   p.partition_size = num_kv_splits ? 0 : partition_size;
   p.splits = num_kv_splits;
   dim3 grid(max_num_partitions, args->num_kv_heads * p.head_groups, args->num_seqs);
+  if (use_tensor_memory_kernel(args))
+    return pkv::launch_attention_fp8_tc(args, p, grid, reinterpret_cast<cudaStream_t>(stream));
   const int64_t units = int64_t(max_num_partitions) * grid.y * args->num_seqs;
   const int w = pick_warps(args, units, num_kv_splits ? Pass::kSplits : Pass::kFixed,
                            partition_size);

@@ -18,6 +18,13 @@ pkv_status_t launch_attention(pkv_dtype_t dtype, pkv_kv_cache_dtype_t kv, const 
                               int head_size, int block_size, int warps, dim3 grid,
                               cudaStream_t stream);
 
+// fp8 caches with head size 128 and block size 16 and f16/bf16 queries run on
+// the tensor-memory kernel (attention_fp8_tc.cuh): fp8_tc_eligible tells,
+// launch_attention_fp8_tc launches it.
+bool fp8_tc_eligible(const pkv_decode_args_t *args);
+pkv_status_t launch_attention_fp8_tc(const pkv_decode_args_t *args, const AttnParams &p, dim3 grid,
+                                     cudaStream_t stream);
+
 // The host-side argument checks of paged_attention_v2_partition (everything
 // but its three scratch pointers), shared with the entry points built on it.
 pkv_status_t check_partition_args(const pkv_decode_args_t *args, int32_t max_num_partitions,

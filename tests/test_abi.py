@@ -238,6 +238,9 @@ def test_reduce_and_metadata_reject_bad_arguments(lib):
     assert lib.pkv_test_set_unarrived_bytes(0) == 0
     assert lib.pkv_set_attention_warps(3) == 1
     assert lib.pkv_set_attention_warps(0) == 0
+    assert lib.pkv_set_fp8_kernel(2) == 1
+    assert lib.pkv_set_fp8_kernel(-1) == 1
+    assert lib.pkv_set_fp8_kernel(0) == 0
 
 
 def test_binding_refuses_host_tensors():
