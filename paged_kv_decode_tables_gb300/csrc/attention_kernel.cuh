@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
   __syncwarp();
 
   const int ntok = int(t1 - t0);
+  const int t0i = int(t0), t1i = int(t1);  // token bounds (below 2^31)
   const int nchunks = (ntok + CH - 1) / CH;
   const int my_n = nchunks > warp ? (nchunks - warp + WARPS - 1) / WARPS : 0;
   const int64_t page0 = t0 / BS;
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
 #pragma unroll
     for (int dt = 0; dt < DT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};
+    float muse[2] = {0.f, 0.f};  // m_run, or 0 while it is -inf
     float l_run[2] = {0.f, 0.f};
 
     const int jm = lane >> 3, rr = lane & 7;
@@ -371,9 +373,9 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
         break;
       }
       waited = i + 1;
-      const int64_t c = warp + int64_t(WARPS) * i;
-      const int nv = int(min(int64_t(CH), t1 - (t0 + c * CH)));
-      const int pb = int(t0 + c * CH) - L + 1;  // ALiBi position of the chunk's token 0
+      const int tok0 = t0i + (warp + WARPS * i) * CH;  // the chunk's first token
+      const int nv = min(CH, t1i - tok0);
+      const int pb = tok0 - L + 1;  // ALiBi position of the chunk's token 0
       uint8_t *ks = wbase + st * Cfg::kStageBytes;
       uint8_t *vs = ks + Cfg::kHalfStage;
       if (nv < CH) {
@@ -415,24 +417,44 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           x[mt][e] = t < nv ? v : -INFINITY;
         }
       }
-      float mloc[2] = {-INFINITY, -INFINITY};
+      // The running max moves only where some lane's score exceeds it: then
+      // the column maxima are reduced over the 8 lanes that hold a head's
+      // tokens and sums and accumulators are rescaled.  Otherwise every
+      // rescale factor would be exactly 1, and the chunk skips the reduction,
+      // its shuffle latency and the rescale (same results either way).
+      float alpha[2] = {1.f, 1.f};
+      bool grow = false;
 #pragma unroll
-      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
-        mloc[0] = fmaxf(mloc[0], fmaxf(x[mt][0], x[mt][2]));
-        mloc[1] = fmaxf(mloc[1], fmaxf(x[mt][1], x[mt][3]));
-      }
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt)
+        grow |= fmaxf(x[mt][0], x[mt][2]) > m_run[0] || fmaxf(x[mt][1], x[mt][3]) > m_run[1];
+      if (__any_sync(FULL, grow)) {
+        float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mloc[0] = fmaxf(mloc[0], __shfl_xor_sync(FULL, mloc[0], o));
-        mloc[1] = fmaxf(mloc[1], __shfl_xor_sync(FULL, mloc[1], o));
-      }
-      float alpha[2], muse[2];
+        for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+          mloc[0] = fmaxf(mloc[0], fmaxf(x[mt][0], x[mt][2]));
+          mloc[1] = fmaxf(mloc[1], fmaxf(x[mt][1], x[mt][3]));
+        }
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float mn = fmaxf(m_run[j], mloc[j]);
-        muse[j] = mn == -INFINITY ? 0.f : mn;
-        alpha[j] = ex2(m_run[j] - muse[j]);
-        m_run[j] = mn;
+        for (int o = 4; o < 32; o <<= 1) {
+          mloc[0] = fmaxf(mloc[0], __shfl_xor_sync(FULL, mloc[0], o));
+          mloc[1] = fmaxf(mloc[1], __shfl_xor_sync(FULL, mloc[1], o));
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float mn = fmaxf(m_run[j], mloc[j]);
+          muse[j] = mn == -INFINITY ? 0.f : mn;
+          alpha[j] = ex2(m_run[j] - muse[j]);
+          m_run[j] = mn;
+        }
+        if (__any_sync(FULL, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+          for (int dt = 0; dt < DT; ++dt) {
+            acc[dt][0] *= alpha[0];
+            acc[dt][1] *= alpha[1];
+            acc[dt][2] *= alpha[0];
+            acc[dt][3] *= alpha[1];
+          }
+        }
       }
       float pr[Cfg::kMTiles][4];
 #pragma unroll
@@ -448,17 +470,6 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       }
       l_run[0] = l_run[0] * alpha[0] + ls0;
       l_run[1] = l_run[1] * alpha[1] + ls1;
-      // alpha is exactly 1 wherever the running max did not grow; once it
-      // settles, whole chunks skip the rescale (x 1 would change nothing).
-      if (__any_sync(FULL, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-        for (int dt = 0; dt < DT; ++dt) {
-          acc[dt][0] *= alpha[0];
-          acc[dt][1] *= alpha[1];
-          acc[dt][2] *= alpha[0];
-          acc[dt][3] *= alpha[1];
-        }
-      }
 #pragma unroll
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
         const uint32_t hi0 = pack2<T>(pr[mt][0], pr[mt][1]);
@@ -564,6 +575,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
 #pragma unroll
     for (int dt = 0; dt < DT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};
+    float muse[2] = {0.f, 0.f};  // m_run, or 0 while it is -inf
     float l_run[2] = {0.f, 0.f};
 
     // Score row gid holds token rA of each 16-token tile, row gid+8 token rA+2,
@@ -578,9 +590,9 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
         break;
       }
       waited = i + 1;
-      const int64_t c = warp + int64_t(WARPS) * i;
-      const int nv = int(min(int64_t(CH), t1 - (t0 + c * CH)));
-      const int pb = int(t0 + c * CH) - L + 1;  // ALiBi position of the chunk's token 0
+      const int tok0 = t0i + (warp + WARPS * i) * CH;  // the chunk's first token
+      const int nv = min(CH, t1i - tok0);
+      const int pb = tok0 - L + 1;  // ALiBi position of the chunk's token 0
       uint8_t *ks = wbase + st * Cfg::kStageBytes;
       uint8_t *vs = ks + Cfg::kHalfStage;
       if (nv < CH) {
@@ -628,24 +640,44 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           x[mt][e] = t < nv ? v : -INFINITY;
         }
       }
-      float mloc[2] = {-INFINITY, -INFINITY};
+      // The running max moves only where some lane's score exceeds it: then
+      // the column maxima are reduced over the 8 lanes that hold a head's
+      // tokens and sums and accumulators are rescaled.  Otherwise every
+      // rescale factor would be exactly 1, and the chunk skips the reduction,
+      // its shuffle latency and the rescale (same results either way).
+      float alpha[2] = {1.f, 1.f};
+      bool grow = false;
 #pragma unroll
-      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
-        mloc[0] = fmaxf(mloc[0], fmaxf(x[mt][0], x[mt][2]));
-        mloc[1] = fmaxf(mloc[1], fmaxf(x[mt][1], x[mt][3]));
-      }
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt)
+        grow |= fmaxf(x[mt][0], x[mt][2]) > m_run[0] || fmaxf(x[mt][1], x[mt][3]) > m_run[1];
+      if (__any_sync(FULL, grow)) {
+        float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mloc[0] = fmaxf(mloc[0], __shfl_xor_sync(FULL, mloc[0], o));
-        mloc[1] = fmaxf(mloc[1], __shfl_xor_sync(FULL, mloc[1], o));
-      }
-      float alpha[2], muse[2];
+        for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+          mloc[0] = fmaxf(mloc[0], fmaxf(x[mt][0], x[mt][2]));
+          mloc[1] = fmaxf(mloc[1], fmaxf(x[mt][1], x[mt][3]));
+        }
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float mn = fmaxf(m_run[j], mloc[j]);
-        muse[j] = mn == -INFINITY ? 0.f : mn;
-        alpha[j] = ex2(m_run[j] - muse[j]);
-        m_run[j] = mn;
+        for (int o = 4; o < 32; o <<= 1) {
+          mloc[0] = fmaxf(mloc[0], __shfl_xor_sync(FULL, mloc[0], o));
+          mloc[1] = fmaxf(mloc[1], __shfl_xor_sync(FULL, mloc[1], o));
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float mn = fmaxf(m_run[j], mloc[j]);
+          muse[j] = mn == -INFINITY ? 0.f : mn;
+          alpha[j] = ex2(m_run[j] - muse[j]);
+          m_run[j] = mn;
+        }
+        if (__any_sync(FULL, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+          for (int dt = 0; dt < DT; ++dt) {
+            acc[dt][0] *= alpha[0];
+            acc[dt][1] *= alpha[1];
+            acc[dt][2] *= alpha[0];
+            acc[dt][3] *= alpha[1];
+          }
+        }
       }
       float pr[Cfg::kMTiles][4];
 #pragma unroll
@@ -661,17 +693,6 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       }
       l_run[0] = l_run[0] * alpha[0] + ls0;
       l_run[1] = l_run[1] * alpha[1] + ls1;
-      // alpha is exactly 1 wherever the running max did not grow; once it
-      // settles, whole chunks skip the rescale (x 1 would change nothing).
-      if (__any_sync(FULL, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-        for (int dt = 0; dt < DT; ++dt) {
-          acc[dt][0] *= alpha[0];
-          acc[dt][1] *= alpha[1];
-          acc[dt][2] *= alpha[0];
-          acc[dt][3] *= alpha[1];
-        }
-      }
 #pragma unroll
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
         // Probabilities x 256 (exact) keep small ones out of f16 subnormals;
