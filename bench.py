@@ -580,7 +580,7 @@ def run_reference(args):
 # long-context split-KV, the tiny worked example) and the fp8-cache and ALiBi
 # variants of the hot path.
 COMPANION_WORKLOADS = ("mha_v1_fp16", "gqa_v1_bf16", "long_v2_bf16", "ragged_v2_fp8",
-                       "long_v2_fp8", "mha_v1_alibi_fp16", "tiny_mha_fp32")
+                       "long_v2_fp8", "mha_v1_alibi_fp16", "tiny_mha_fp32", "gqa_v1_fp32")
 # Workloads whose oracle is also timed on one core (the small and mid-size
 # configurations); the headline's oracle runs on every core.
 ONE_CORE_WORKLOADS = ("tiny_mha_fp32", "mha_v1_fp16", "gqa_v1_bf16")

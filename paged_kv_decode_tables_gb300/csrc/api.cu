@@ -156,7 +156,10 @@ AttnParams make_params(const pkv_decode_args_t *a) {
 // - split-KV with enough units to fill every SM many times over: 1 for fixed
 //   partitions of at most 512 tokens (short, even units), 2 for split counts
 //   or longer partitions (units can be long and uneven);
-// - split-KV with few units: 4.
+// - split-KV with few units: 4;
+// - fp32 caches: at most 2 (a warp's two 16-token stages take 32 KiB at head
+//   size 128, so 4-warp CTAs leave one CTA and 4 warps per SM: the fp32 GQA
+//   single pass ran 0.60 of the copy bandwidth on 4 warps, 0.90 on 2).
 enum class Pass { kSingle, kFixed, kSplits };
 
 int pick_warps(const pkv_decode_args_t *a, int64_t units, Pass pass, int partition_size) {
@@ -172,6 +175,7 @@ int pick_warps(const pkv_decode_args_t *a, int64_t units, Pass pass, int partiti
     want = 1;
   else
     want = 2;
+  if (a->dtype == PKV_F32 && want > 2) want = 2;
   while (want > 1 && !have(want)) want /= 2;
   return want;
 }

@@ -33,7 +33,9 @@
 // domain with ex2; row maxima use warp shuffles; a chunk in which no running
 // max grew skips the accumulator rescale (its factor would be exactly 1).
 //
-// fp32 runs the same pipeline with a CUDA-core body (no fp32 tensor path).
+// fp32 runs the same pipeline with both products on tf32 MMAs, each operand
+// split into two tf32 terms (three MMAs per tile), which keeps the products
+// close to fp32 rounding.
 //
 // fp8 caches (E4M3 / E5M2 codes, one byte per element; page
 // "paged_attention_v2_triton.py" names kv_cache_dtype, k_scale and v_scale in
@@ -120,11 +122,17 @@ struct AttnCfg {
   static constexpr int kStages = 2;
   static constexpr int kWarpBytes = kStages * kStageBytes;
   static constexpr int kEpiFloats = kMaxGroup * D + 2 * kMaxGroup;
-  static constexpr int kSmemBytes = WARPS * kWarpBytes + WARPS * kStages * 8;
+  // fp32 caches: per-warp probabilities of one chunk, [head][token] with rows
+  // of kChunk + 4 floats (the padding spreads a row's stores over the banks).
+  static constexpr int kPRow = kChunk + 4;
+  static constexpr int kPBytes = kElem == 4 ? kMaxGroup * kPRow * 4 : 0;
+  static constexpr int kBarOffset = WARPS * (kWarpBytes + kPBytes);
+  static constexpr int kSmemBytes = kBarOffset + WARPS * kStages * 8;
   static constexpr int kThreads = WARPS * 32;
   static_assert(kEpiFloats * 4 <= kWarpBytes, "epilogue does not fit the warp's stages");
   static_assert(D % 32 == 0 && BS % 8 == 0, "unsupported shape");
   static_assert(kHalfStage % 16 == 0 && kPageBytes % 16 == 0, "bulk copies need 16 B");
+  static_assert(kPBytes % 16 == 0 && (kPRow * 4) % 16 == 0, "16-byte probability rows");
 };
 
 // CTAs per SM an instance is compiled to keep resident (0: no floor), all
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
   // -------------------------------------------------------------- pipeline --
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *wbase = smem + warp * Cfg::kWarpBytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * Cfg::kWarpBytes) + warp * NST;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOffset) + warp * NST;
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
@@ -774,28 +782,55 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
     }
   } else {
-    // ------------------------------------------------ fp32 CUDA-core body --
-    constexpr int DL = D / 32;  // dims per lane: lane + 32*i
-    float qv[kMaxGroup][DL];
-    float acc[kMaxGroup][DL];
-    float m_run[kMaxGroup], l_run[kMaxGroup];
+    // ------------------------------------------- fp32, 3xTF32 tensor body --
+    // Both products on mma.sync m16n8k8 tf32.  Every operand x is split as
+    // hi + lo (split_tf32: two tf32 values, |x - hi - lo| <= 2^-22 |x|) and
+    // a product ab is taken as hi_a hi_b + hi_a lo_b + lo_a hi_b, leaving out
+    // lo_a lo_b (<= 2^-22 |ab|): close to fp32 rounding at three MMAs per tile.
+    // Scores S^T = K Q^T: M = 16 tokens, N = 8 heads, K = 8 dims; ldmatrix
+    // reads the key page (16-byte rows = 4 dims of one token): matrices
+    // (tokens 0-7 | 8-15) x (dims 8kk..8kk+3 | 8kk+4..8kk+7) are exactly the
+    // tf32 A fragment, k-slot c = dim 8kk + c.  Output O^T = V^T P^T: M = 16
+    // head dims, N = 8 heads, K = 8 tokens; each lane reads 4 consecutive
+    // tokens 4tig..4tig+3 of one dim row of the value page in 16 bytes and
+    // puts them on k-slots (tig, tig+4) of two MMAs: k-step 0 takes tokens
+    // 4tig and 4tig+1, k-step 1 tokens 4tig+2 and 4tig+3.  The probabilities
+    // reach that order through a per-warp [head][token] array in shared
+    // memory.
+    constexpr int DK = D / 8;   // 8-dim k-steps of the key product
+    constexpr int DT = D / 16;  // 16-dim tiles of the value product
+    const int gid = lane >> 2, tig = lane & 3;
+    // Query fragments (B operand): head gid, dims 8kk + tig and 8kk + tig + 4.
+    uint32_t qh[DK][2], ql[DK][2];
     {
-      const float *qb = static_cast<const float *>(p.q) + int64_t(seq) * p.q_s0;
+      const float *qb = static_cast<const float *>(p.q) + int64_t(seq) * p.q_s0 +
+                        int64_t(h0 + gid) * p.q_s1;
 #pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) {
+      for (int kk = 0; kk < DK; ++kk) {
 #pragma unroll
-        for (int i = 0; i < DL; ++i) {
-          qv[h][i] = h < g ? qb[int64_t(h0 + h) * p.q_s1 + int64_t(lane + 32 * i) * p.q_s2] : 0.f;
-          acc[h][i] = 0.f;
+        for (int j = 0; j < 2; ++j) {
+          const float v = gid < g ? qb[int64_t(8 * kk + tig + 4 * j) * p.q_s2] : 0.f;
+          split_tf32(v, qh[kk][j], ql[kk][j]);
         }
-        m_run[h] = -INFINITY;
-        l_run[h] = 0.f;
       }
     }
-    float slh[kMaxGroup];  // ALiBi slopes, log2 units
+    float sl2[2] = {0.f, 0.f};  // ALiBi slopes (log2 units) of heads 2tig, 2tig+1
+    if (p.alibi != nullptr) {
 #pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h)
-      slh[h] = (p.alibi != nullptr && h < g) ? p.alibi[h0 + h] * kLog2e : 0.f;
+      for (int j = 0; j < 2; ++j) {
+        const int h = 2 * tig + j;
+        if (h < g) sl2[j] = p.alibi[h0 + h] * kLog2e;
+      }
+    }
+    float acc[DT][4];
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float muse[2] = {0.f, 0.f};  // m_run, or 0 while it is -inf
+    float l_run[2] = {0.f, 0.f};
+    float *pw = reinterpret_cast<float *>(smem + WARPS * Cfg::kWarpBytes + warp * Cfg::kPBytes);
+
+    const int jm = lane >> 3, rr = lane & 7;
     for (int i = 0; i < my_n; ++i) {
       const int st = i % NST;
       const bool got = mbar_wait_bounded(&bars[st], uint32_t(i / NST) & 1u, p.wait_limit_ns);
@@ -804,61 +839,158 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
         break;
       }
       waited = i + 1;
-      const int64_t c = warp + int64_t(WARPS) * i;
-      const int nv = int(min(int64_t(CH), t1 - (t0 + c * CH)));
-      const int pb = int(t0 + c * CH) - L + 1;
-      const float *kf = reinterpret_cast<const float *>(wbase + st * Cfg::kStageBytes);
-      const float *vf = kf + CH * D;
-      // The chunk's tokens accumulate into chunk-local sums (cacc, cl) while
-      // cs collects the chunk's rescale factors for the running ones, which
-      // then take one addition per chunk instead of one per token: the fp32
-      // rounding of a long sequence grows with its chunk count, not its length.
-      float cacc[kMaxGroup][DL], cl[kMaxGroup], cs[kMaxGroup];
-#pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) {
-#pragma unroll
-        for (int i2 = 0; i2 < DL; ++i2) cacc[h][i2] = 0.f;
-        cl[h] = 0.f;
-        cs[h] = 1.f;
+      const int tok0 = t0i + (warp + WARPS * i) * CH;  // the chunk's first token
+      const int nv = min(CH, t1i - tok0);
+      const int pb = tok0 - L + 1;  // ALiBi position of the chunk's token 0
+      uint8_t *ks = wbase + st * Cfg::kStageBytes;
+      uint8_t *vs = ks + Cfg::kHalfStage;
+      if (nv < CH) {
+        // Zero the value columns of tokens past the end: their probability
+        // is 0, but 0 * (stale or NaN) must not reach the accumulator.
+        float *vt = reinterpret_cast<float *>(vs);
+        const int ntail = CH - nv;
+        for (int e = lane; e < D * ntail; e += 32) {
+          const int d = e / ntail;
+          const int tau = nv + e % ntail;
+          vt[(tau / BS) * (D * BS) + d * BS + (tau % BS)] = 0.f;
+        }
+        __syncwarp();
       }
-      for (int tau = 0; tau < nv; ++tau) {
-        const int pg = tau / BS, slot = tau % BS;
-        float kv[DL], vv[DL];
+      const uint32_t ks_a = smem_addr(ks);
+
+      float x[Cfg::kMTiles][4];
 #pragma unroll
-        for (int i2 = 0; i2 < DL; ++i2) {
-          const int d = lane + 32 * i2;
-          kv[i2] = kf[pg * (D * BS) + (d / 4) * (BS * 4) + slot * 4 + (d & 3)];
-          vv[i2] = vf[pg * (D * BS) + d * BS + slot];
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        // Two accumulators for the leading terms, two for the corrections
+        // (even / odd k-steps), summed small-first.
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int tok = 16 * mt + rr + 8 * (jm & 1);
+        const uint32_t rowa =
+            ks_a + (tok / BS) * Cfg::kPageBytes + ((jm >> 1) * BS + (tok % BS)) * 16;
+#pragma unroll
+        for (int kk = 0; kk < DK; ++kk) {
+          uint32_t a[4], ah[4], al[4];
+          ldsm_x4(rowa + kk * (2 * BS * 16), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_tf32_fast(__uint_as_float(a[e]), ah[e], al[e]);
+          float(&sa)[4] = (kk & 1) ? s1 : s0;
+          float(&ca)[4] = (kk & 1) ? c1 : c0;
+          mma_tf32_16808(ca, al[0], al[1], al[2], al[3], qh[kk][0], qh[kk][1]);
+          mma_tf32_16808(ca, ah[0], ah[1], ah[2], ah[3], ql[kk][0], ql[kk][1]);
+          mma_tf32_16808(sa, ah[0], ah[1], ah[2], ah[3], qh[kk][0], qh[kk][1]);
         }
 #pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
-          if (h < g) {
-            float part = 0.f;
+        for (int e = 0; e < 4; ++e) {
+          const int t = 16 * mt + gid + 8 * (e >> 1);
+          float v = ((c0[e] + c1[e]) + (s0[e] + s1[e])) * p.scale_log2;
+          if (p.alibi != nullptr) v = fmaf(sl2[e & 1], float(pb + t), v);
+          x[mt][e] = t < nv ? v : -INFINITY;
+        }
+      }
+      // Running max and probabilities as in the 16-bit body; the rescale
+      // joins the chunk's sums below.
+      float alpha[2] = {1.f, 1.f};
+      bool grow = false;
 #pragma unroll
-            for (int i2 = 0; i2 < DL; ++i2) part = fmaf(qv[h][i2], kv[i2], part);
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt)
+        grow |= fmaxf(x[mt][0], x[mt][2]) > m_run[0] || fmaxf(x[mt][1], x[mt][3]) > m_run[1];
+      if (__any_sync(FULL, grow)) {
+        float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
-            float xs = part * p.scale_log2;
-            if (p.alibi != nullptr) xs = fmaf(slh[h], float(pb + tau), xs);
-            const float mn = fmaxf(m_run[h], xs);
-            const float a = ex2(m_run[h] - mn);
-            const float pe = ex2(xs - mn);
-            cl[h] = cl[h] * a + pe;
-            cs[h] *= a;
+        for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+          mloc[0] = fmaxf(mloc[0], fmaxf(x[mt][0], x[mt][2]));
+          mloc[1] = fmaxf(mloc[1], fmaxf(x[mt][1], x[mt][3]));
+        }
 #pragma unroll
-            for (int i2 = 0; i2 < DL; ++i2) cacc[h][i2] = fmaf(cacc[h][i2], a, pe * vv[i2]);
-            m_run[h] = mn;
+        for (int o = 4; o < 32; o <<= 1) {
+          mloc[0] = fmaxf(mloc[0], __shfl_xor_sync(FULL, mloc[0], o));
+          mloc[1] = fmaxf(mloc[1], __shfl_xor_sync(FULL, mloc[1], o));
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float mn = fmaxf(m_run[j], mloc[j]);
+          muse[j] = mn == -INFINITY ? 0.f : mn;
+          alpha[j] = ex2(m_run[j] - muse[j]);
+          m_run[j] = mn;
+        }
+      }
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pr = ex2(x[mt][e] - muse[e & 1]);
+          if (e & 1)
+            ls1 += pr;
+          else
+            ls0 += pr;
+          pw[(2 * tig + (e & 1)) * Cfg::kPRow + 16 * mt + gid + 8 * (e >> 1)] = pr;
+        }
+      }
+      l_run[0] = l_run[0] * alpha[0] + ls0;
+      l_run[1] = l_run[1] * alpha[1] + ls1;
+      __syncwarp();
+      // The chunk's value products accumulate from zero and join the running
+      // sums with one fp32 FMA each (acc * alpha + chunk): the tensor core's
+      // accumulation does not round to nearest, so adding every MMA into a
+      // long-lived accumulator would let its rounding grow with the length.
+      float cacc[DT][4];
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) cacc[dt][0] = cacc[dt][1] = cacc[dt][2] = cacc[dt][3] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        // B fragments: head gid, tokens 16mt + 4tig + {0, 1} (k-step 0) and
+        // + {2, 3} (k-step 1).
+        const float4 pq = *reinterpret_cast<const float4 *>(pw + gid * Cfg::kPRow + 16 * mt +
+                                                            4 * tig);
+        uint32_t ph[4], pl[4];
+        split_tf32_fast(pq.x, ph[0], pl[0]);
+        split_tf32_fast(pq.y, ph[1], pl[1]);
+        split_tf32_fast(pq.z, ph[2], pl[2]);
+        split_tf32_fast(pq.w, ph[3], pl[3]);
+        const int tv = 16 * mt + 4 * tig;
+        const float *vrow = reinterpret_cast<const float *>(vs + (tv / BS) * Cfg::kPageBytes) +
+                            gid * BS + (tv % BS);
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          const float4 va = *reinterpret_cast<const float4 *>(vrow + (16 * dt) * BS);
+          const float4 vb = *reinterpret_cast<const float4 *>(vrow + (16 * dt + 8) * BS);
+          uint32_t ah[8], al[8];
+          split_tf32_fast(va.x, ah[0], al[0]);
+          split_tf32_fast(vb.x, ah[1], al[1]);
+          split_tf32_fast(va.y, ah[2], al[2]);
+          split_tf32_fast(vb.y, ah[3], al[3]);
+          split_tf32_fast(va.z, ah[4], al[4]);
+          split_tf32_fast(vb.z, ah[5], al[5]);
+          split_tf32_fast(va.w, ah[6], al[6]);
+          split_tf32_fast(vb.w, ah[7], al[7]);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int o = 4 * k;
+            mma_tf32_16808(cacc[dt], al[o], al[o + 1], al[o + 2], al[o + 3], ph[2 * k],
+                           ph[2 * k + 1]);
+            mma_tf32_16808(cacc[dt], ah[o], ah[o + 1], ah[o + 2], ah[o + 3], pl[2 * k],
+                           pl[2 * k + 1]);
+            mma_tf32_16808(cacc[dt], ah[o], ah[o + 1], ah[o + 2], ah[o + 3], ph[2 * k],
+                           ph[2 * k + 1]);
           }
         }
       }
 #pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) {
-        l_run[h] = fmaf(l_run[h], cs[h], cl[h]);
+      for (int dt = 0; dt < DT; ++dt) {
 #pragma unroll
-        for (int i2 = 0; i2 < DL; ++i2) acc[h][i2] = fmaf(acc[h][i2], cs[h], cacc[h][i2]);
+        for (int e = 0; e < 4; ++e) acc[dt][e] = fmaf(acc[dt][e], alpha[e & 1], cacc[dt][e]);
       }
       __syncwarp();
       if (issued < my_n) issue_next();
+    }
+
+    // Full per-head sums: lanes sharing lane%4 hold the same two heads.
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l_run[0] += __shfl_xor_sync(FULL, l_run[0], o);
+      l_run[1] += __shfl_xor_sync(FULL, l_run[1], o);
     }
     if (!ok) {
       if (lane == 0) flag_error(p.err, 16u);
@@ -868,16 +1000,19 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       __syncwarp();
     }
 #pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) {
+    for (int dt = 0; dt < DT; ++dt) {
 #pragma unroll
-      for (int i = 0; i < DL; ++i) epi[h * D + lane + 32 * i] = acc[h][i];
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) {
-        epi[kMaxGroup * D + h] = m_run[h];
-        epi[kMaxGroup * D + kMaxGroup + h] = l_run[h];
+      for (int e = 0; e < 4; ++e) {
+        const int d = 16 * dt + gid + 8 * (e >> 1);
+        const int h = 2 * tig + (e & 1);
+        epi[h * D + d] = acc[dt][e];
       }
+    }
+    if (lane < 4) {
+      epi[kMaxGroup * D + 2 * lane] = m_run[0];
+      epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
+      epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
+      epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
     }
   }
 

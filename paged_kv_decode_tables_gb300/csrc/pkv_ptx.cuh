@@ -1,6 +1,6 @@
 // Inline-PTX building blocks for the sm_103a decode kernels: mbarrier-tracked
-// bulk copies (global -> shared), bounded barrier waits, ldmatrix / movmatrix
-// and the m16n8k16 tensor-core MMA.
+// bulk copies (global -> shared), bounded barrier waits, ldmatrix / movmatrix,
+// the m16n8k16 (f16 / bf16) and m16n8k8 (tf32) tensor-core MMAs.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -149,6 +149,41 @@ struct Mma16816<__half> {
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
 };
+
+// D += A B on tf32 operands (m16n8k8): A row-major 16x8, B column-major 8x8,
+// each operand element one 32-bit register holding a tf32 value.
+__device__ __forceinline__ void mma_tf32_16808(float (&c)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// x rounded to tf32 (nearest, ties away from zero), as fp32 bits with the
+// low 13 mantissa bits zero.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// x = hi + lo + e, hi and lo tf32, |e| <= 2^-22 |x| (for finite x): hi is x
+// rounded to 11 significant bits, x - hi is exact in fp32 and is rounded again.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+
+// The same split with lo left unrounded: a tf32 MMA takes the top 19 bits
+// of each operand register, so lo enters with at most 2^-10 |lo| <= 2^-21
+// |x| error, one conversion fewer per element.
+__device__ __forceinline__ void split_tf32_fast(float x, uint32_t &hi, uint32_t &lo) {
+  hi = to_tf32(x);
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
 
 // 2^x on the SFU (relative error ~2^-22); ex2(-inf) = 0.
 __device__ __forceinline__ float ex2(float x) {

@@ -222,6 +222,26 @@ def test_unused_cache_slots_never_reach_the_output():
     assert_attention_close(run_v1(on_device(inp32)), _oracle_v1(inp32), torch.float32, "NaN f32")
 
 
+@pytest.mark.parametrize("D,bs", [(64, 16), (128, 8), (128, 32)])
+def test_fp32_long_sequences_keep_the_fp32_bound(D, bs):
+    """fp32 on the tf32 tensor path: one warp walks a whole long sequence (up
+    to 9000 tokens, 1 % of keys x8), so the running sums take hundreds of
+    chunks; the output stays within the 1e-5 fp32 bound, single pass and
+    split-KV."""
+    lens = [597, 4099, 9000, 33]
+    inp = _inputs("f32", D, bs, 8, 2, lens, seed=23, peaky_fraction=0.01, peaky_scale=8.0)
+    g = on_device(inp)
+    ref = _oracle_v1(inp)
+    pkv.set_attention_warps(1)
+    try:
+        assert_attention_close(run_v1(g), ref, torch.float32, f"fp32 long D{D} bs{bs} v1")
+        maxP = -(-inp["max_blocks_per_seq"] * bs // 4096)
+        _, _, _, out = run_v2(g, maxP, partition_size=4096)
+        assert_attention_close(out, ref, torch.float32, f"fp32 long D{D} bs{bs} v2")
+    finally:
+        pkv.set_attention_warps(0)
+
+
 def test_zero_length_sequences():
     lens = [0, 5, 0, 300]
     inp = _inputs("bf16", 128, 16, 8, 2, lens, seed=18)

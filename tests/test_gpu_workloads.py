@@ -55,7 +55,7 @@ def _value_range(inp):
 
 @pytest.mark.parametrize("name", ["mha_v1_fp16", "gqa_v1_bf16", "long_v2_bf16", "ragged_v2_bf16",
                                   "tiny_mha_fp32", "ragged_v2_fp8", "long_v2_fp8",
-                                  "mha_v1_alibi_fp16"])
+                                  "mha_v1_alibi_fp16", "gqa_v1_fp32"])
 def test_full_size_workload(name):
     step = _run_step(name)
     inp, spec = step.inp, step.spec

@@ -118,6 +118,14 @@ WORKLOADS: Dict[str, WorkloadSpec] = {
         num_seqs=256, num_heads=32, num_kv_heads=8, head_size=128, block_size=16, dtype="bf16",
         seq_len_recipe="uniform", seq_len_lo=128, seq_len_hi=2048, mode="v1",
     ),
+    "gqa_v1_fp32": WorkloadSpec(
+        name="gqa_v1_fp32",
+        description=("GQA single-pass decode, fp32: the GQA batch (256 seqs, 32 query heads / 8 kv "
+                     "heads, head_size 128, block_size 16, seq_lens uniform in [128, 2048]) with "
+                     "fp32 queries, caches and output"),
+        num_seqs=256, num_heads=32, num_kv_heads=8, head_size=128, block_size=16, dtype="f32",
+        seq_len_recipe="uniform", seq_len_lo=128, seq_len_hi=2048, mode="v1",
+    ),
     "long_v2_bf16": WorkloadSpec(
         name="long_v2_bf16",
         description=("long-context split-KV decode, bf16: 8 seqs of 16k..128k tokens, 64 query heads / "
