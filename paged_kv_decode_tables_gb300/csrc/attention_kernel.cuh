@@ -535,13 +535,20 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     // ------------------------------------- fp8 cache, f16 tensor-core body --
     constexpr int DT = D / 16;
     const int gid = lane >> 2, tig = lane & 3;
-    // Query fragments (B operand, f16) of head gid: dims 16ks + 4tig + {0, 1}
+    // Column pairs: with at most 4 heads in the CTA, head h takes MMA column
+    // 2h of the score product (column 2h + 1 has a zero query), and in the
+    // value product columns 2h and 2h + 1 carry the hi and lo parts of head
+    // h's probabilities, so one MMA does what the hi and lo MMAs do otherwise.
+    // A lane then holds one head (tig) instead of two.
+    const bool pair = g <= 4;
+    // Query fragments (B operand, f16) of column gid: dims 16ks + 4tig + {0, 1}
     // on k-slots 2tig, 2tig+1 and dims 16ks + 4tig + {2, 3} on 2tig+8, 2tig+9.
     uint32_t qf[DT][2];
-    float head_unscale;  // 2^-k: undoes the f16 range scale 2^k of head gid's query
+    float head_unscale;  // 2^-k: undoes the f16 range scale 2^k of column gid's query
     {
+      const int qh = pair ? ((gid & 1) ? kMaxGroup : (gid >> 1)) : gid;  // head of column gid
       const T *qb = static_cast<const T *>(p.q) + int64_t(seq) * p.q_s0 +
-                    int64_t(h0 + gid) * p.q_s1;
+                    int64_t(h0 + min(qh, g - 1)) * p.q_s1;
       float qv[DT][4];
       float amax = 0.f;
 #pragma unroll
@@ -549,7 +556,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int d = 16 * ks + 4 * tig + j;
-          qv[ks][j] = gid < g ? to_f32<T>(qb[int64_t(d) * p.q_s2]) : 0.f;
+          qv[ks][j] = qh < g ? to_f32<T>(qb[int64_t(d) * p.q_s2]) : 0.f;
           amax = fmaxf(amax, fabsf(qv[ks][j]));
         }
       }
@@ -571,12 +578,14 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       }
     }
     // Logit factor and ALiBi slope (log2 units) of this lane's two score
-    // columns, heads 2tig and 2tig+1 (head h's query is on lanes 4h..4h+3).
+    // columns 2tig and 2tig+1 (column c's query is on lanes 4c..4c+3): heads
+    // 2tig and 2tig+1, or with column pairs head tig and a column not used.
     float xs2[2], sl2[2] = {0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int h = 2 * tig + j;
-      xs2[j] = p.scale_log2 * __shfl_sync(FULL, head_unscale, 4 * h);
+      const int c = 2 * tig + j;
+      const int h = pair ? (j ? kMaxGroup : tig) : c;
+      xs2[j] = p.scale_log2 * __shfl_sync(FULL, head_unscale, 4 * c);
       if (p.alibi != nullptr && h < g) sl2[j] = p.alibi[h0 + h] * kLog2e;
     }
     float acc[DT][4];
@@ -645,7 +654,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           const int t = 16 * mt + rA + 2 * (e >> 1);
           float v = (s0[e] + s1[e]) * xs2[e & 1];
           if (p.alibi != nullptr) v = fmaf(sl2[e & 1], float(pb + t), v);
-          x[mt][e] = t < nv ? v : -INFINITY;
+          x[mt][e] = (t < nv && !(pair && (e & 1))) ? v : -INFINITY;
         }
       }
       // The running max moves only where some lane's score exceeds it: then
@@ -677,6 +686,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           alpha[j] = ex2(m_run[j] - muse[j]);
           m_run[j] = mn;
         }
+        if (pair) alpha[1] = alpha[0];  // both columns hold head tig's sums
         if (__any_sync(FULL, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
           for (int dt = 0; dt < DT; ++dt) {
@@ -688,10 +698,19 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
         }
       }
       float pr[Cfg::kMTiles][4];
+      if (pair) {
 #pragma unroll
-      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+          pr[mt][0] = ex2(x[mt][0] - muse[0]);
+          pr[mt][2] = ex2(x[mt][2] - muse[0]);
+          pr[mt][1] = pr[mt][3] = 0.f;
+        }
+      } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pr[mt][e] = ex2(x[mt][e] - muse[e & 1]);
+        for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pr[mt][e] = ex2(x[mt][e] - muse[e & 1]);
+        }
       }
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
@@ -705,15 +724,27 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
         // Probabilities x 256 (exact) keep small ones out of f16 subnormals;
         // the epilogue takes the factor back out.
-        const float q0 = pr[mt][0] * 256.f, q1 = pr[mt][1] * 256.f;
-        const float q2 = pr[mt][2] * 256.f, q3 = pr[mt][3] * 256.f;
-        const uint32_t hi0 = pack2<__half>(q0, q1);
-        const uint32_t hi1 = pack2<__half>(q2, q3);
-        const float2 f0 = unpack2<__half>(hi0), f1 = unpack2<__half>(hi1);
-        const uint32_t lo0 = pack2<__half>(q0 - f0.x, q1 - f0.y);
-        const uint32_t lo1 = pack2<__half>(q2 - f1.x, q3 - f1.y);
-        const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
-        const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
+        uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+        if (pair) {
+          // Columns 2tig, 2tig+1 of rows gid and gid+8: head tig's hi and lo.
+          const float q0 = pr[mt][0] * 256.f, q2 = pr[mt][2] * 256.f;
+          const float h0f = __half2float(__float2half_rn(q0));
+          const float h2f = __half2float(__float2half_rn(q2));
+          bh0 = movmatrix_trans(pack2<__half>(q0, q0 - h0f));
+          bh1 = movmatrix_trans(pack2<__half>(q2, q2 - h2f));
+        } else {
+          const float q0 = pr[mt][0] * 256.f, q1 = pr[mt][1] * 256.f;
+          const float q2 = pr[mt][2] * 256.f, q3 = pr[mt][3] * 256.f;
+          const uint32_t hi0 = pack2<__half>(q0, q1);
+          const uint32_t hi1 = pack2<__half>(q2, q3);
+          const float2 f0 = unpack2<__half>(hi0), f1 = unpack2<__half>(hi1);
+          const uint32_t lo0 = pack2<__half>(q0 - f0.x, q1 - f0.y);
+          const uint32_t lo1 = pack2<__half>(q2 - f1.x, q3 - f1.y);
+          bh0 = movmatrix_trans(hi0);
+          bh1 = movmatrix_trans(hi1);
+          bl0 = movmatrix_trans(lo0);
+          bl1 = movmatrix_trans(lo1);
+        }
         if constexpr (BS >= 16) {
           // A value row holds a dim's 16 tokens of the tile in 16 bytes: one
           // ldmatrix.x4 gives the words of dims gid, gid+8 for two dim tiles
@@ -731,7 +762,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
               fp8x4_to_f16x2<KV>(w[2 * h], a[0], a[2]);
               fp8x4_to_f16x2<KV>(w[2 * h + 1], a[1], a[3]);
               Mma16816<__half>::run(acc[dt + h], a, bh0, bh1);
-              Mma16816<__half>::run(acc[dt + h], a, bl0, bl1);
+              if (!pair) Mma16816<__half>::run(acc[dt + h], a, bl0, bl1);
             }
           }
         } else {
@@ -746,7 +777,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
             fp8x4_to_f16x2<KV>(wa, a[0], a[2]);
             fp8x4_to_f16x2<KV>(wb, a[1], a[3]);
             Mma16816<__half>::run(acc[dt], a, bh0, bh1);
-            Mma16816<__half>::run(acc[dt], a, bl0, bl1);
+            if (!pair) Mma16816<__half>::run(acc[dt], a, bl0, bl1);
           }
         }
       }
@@ -766,20 +797,36 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
                           min(p.wait_limit_ns, uint64_t(100000000ull)));
       __syncwarp();
     }
+    if (pair) {
+      // Head tig: the hi and lo columns' sums add up.
 #pragma unroll
-    for (int dt = 0; dt < DT; ++dt) {
+      for (int dt = 0; dt < DT; ++dt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = 16 * dt + gid + 8 * (e >> 1);
-        const int h = 2 * tig + (e & 1);
-        epi[h * D + d] = acc[dt][e] * (1.f / 256.f);
+        for (int r = 0; r < 2; ++r) {
+          const int d = 16 * dt + gid + 8 * r;
+          epi[tig * D + d] = (acc[dt][2 * r] + acc[dt][2 * r + 1]) * (1.f / 256.f);
+        }
       }
-    }
-    if (lane < 4) {
-      epi[kMaxGroup * D + 2 * lane] = m_run[0];
-      epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
-      epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
-      epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
+      if (lane < 4) {
+        epi[kMaxGroup * D + lane] = m_run[0];
+        epi[kMaxGroup * D + kMaxGroup + lane] = l_run[0];
+      }
+    } else {
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = 16 * dt + gid + 8 * (e >> 1);
+          const int h = 2 * tig + (e & 1);
+          epi[h * D + d] = acc[dt][e] * (1.f / 256.f);
+        }
+      }
+      if (lane < 4) {
+        epi[kMaxGroup * D + 2 * lane] = m_run[0];
+        epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
+        epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
+        epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
+      }
     }
   } else {
     // ------------------------------------------- fp32, 3xTF32 tensor body --
@@ -797,28 +844,38 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     // 4tig and 4tig+1, k-step 1 tokens 4tig+2 and 4tig+3.  The probabilities
     // reach that order through a per-warp [head][token] array in shared
     // memory.
+    // Column pairs (at most 4 heads in the CTA): columns 2h and 2h + 1 of
+    // both products carry the hi and lo terms of head h's query (probabilities),
+    // so one MMA per A term covers both B terms: two MMAs per tile instead of
+    // three (and the small lo lo term comes along).  A lane then holds one
+    // head (tig), its score the sum of its two columns.
     constexpr int DK = D / 8;   // 8-dim k-steps of the key product
     constexpr int DT = D / 16;  // 16-dim tiles of the value product
     const int gid = lane >> 2, tig = lane & 3;
-    // Query fragments (B operand): head gid, dims 8kk + tig and 8kk + tig + 4.
+    const bool pair = g <= 4;
+    // Query fragments (B operand): column gid, dims 8kk + tig and 8kk + tig + 4;
+    // with column pairs qh holds column gid's term (hi of head gid/2 for even
+    // gid, lo for odd) and ql is not used.
     uint32_t qh[DK][2], ql[DK][2];
     {
+      const int qhd = pair ? (gid >> 1) : gid;  // head of column gid
       const float *qb = static_cast<const float *>(p.q) + int64_t(seq) * p.q_s0 +
-                        int64_t(h0 + gid) * p.q_s1;
+                        int64_t(h0 + min(qhd, g - 1)) * p.q_s1;
 #pragma unroll
       for (int kk = 0; kk < DK; ++kk) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const float v = gid < g ? qb[int64_t(8 * kk + tig + 4 * j) * p.q_s2] : 0.f;
+          const float v = qhd < g ? qb[int64_t(8 * kk + tig + 4 * j) * p.q_s2] : 0.f;
           split_tf32(v, qh[kk][j], ql[kk][j]);
+          if (pair && (gid & 1)) qh[kk][j] = ql[kk][j];
         }
       }
     }
-    float sl2[2] = {0.f, 0.f};  // ALiBi slopes (log2 units) of heads 2tig, 2tig+1
+    float sl2[2] = {0.f, 0.f};  // ALiBi slopes (log2 units) of this lane's heads
     if (p.alibi != nullptr) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int h = 2 * tig + j;
+        const int h = pair ? (j ? kMaxGroup : tig) : 2 * tig + j;
         if (h < g) sl2[j] = p.alibi[h0 + h] * kLog2e;
       }
     }
@@ -828,6 +885,12 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     float m_run[2] = {-INFINITY, -INFINITY};
     float muse[2] = {0.f, 0.f};  // m_run, or 0 while it is -inf
     float l_run[2] = {0.f, 0.f};
+    // Compensation terms of l_run (Kahan summation).  Once one token holds
+    // most of a head's mass, l_run sits near its final value while a chunk
+    // adds far less than half an ulp of it; plain fp32 adds would drop every
+    // such addition, always in the same direction, so the loss would grow
+    // with the chunks a warp walks (2.4e-5 after 9000 peaky tokens).
+    float l_c[2] = {0.f, 0.f};
     float *pw = reinterpret_cast<float *>(smem + WARPS * Cfg::kWarpBytes + warp * Cfg::kPBytes);
 
     const int jm = lane >> 3, rr = lane & 7;
@@ -877,15 +940,31 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           float(&sa)[4] = (kk & 1) ? s1 : s0;
           float(&ca)[4] = (kk & 1) ? c1 : c0;
           mma_tf32_16808(ca, al[0], al[1], al[2], al[3], qh[kk][0], qh[kk][1]);
-          mma_tf32_16808(ca, ah[0], ah[1], ah[2], ah[3], ql[kk][0], ql[kk][1]);
+          if (!pair) mma_tf32_16808(ca, ah[0], ah[1], ah[2], ah[3], ql[kk][0], ql[kk][1]);
           mma_tf32_16808(sa, ah[0], ah[1], ah[2], ah[3], qh[kk][0], qh[kk][1]);
         }
+        if (pair) {
+          // Column 2tig: hi K x hi q (s) and lo K x hi q (c); column 2tig+1:
+          // the same with lo q.
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = 16 * mt + gid + 8 * (e >> 1);
-          float v = ((c0[e] + c1[e]) + (s0[e] + s1[e])) * p.scale_log2;
-          if (p.alibi != nullptr) v = fmaf(sl2[e & 1], float(pb + t), v);
-          x[mt][e] = t < nv ? v : -INFINITY;
+          for (int r = 0; r < 2; ++r) {
+            const int t = 16 * mt + gid + 8 * r;
+            const float small =
+                ((c0[2 * r + 1] + c1[2 * r + 1]) + (c0[2 * r] + c1[2 * r])) +
+                (s0[2 * r + 1] + s1[2 * r + 1]);
+            float v = (small + (s0[2 * r] + s1[2 * r])) * p.scale_log2;
+            if (p.alibi != nullptr) v = fmaf(sl2[0], float(pb + t), v);
+            x[mt][2 * r] = t < nv ? v : -INFINITY;
+            x[mt][2 * r + 1] = -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = 16 * mt + gid + 8 * (e >> 1);
+            float v = ((c0[e] + c1[e]) + (s0[e] + s1[e])) * p.scale_log2;
+            if (p.alibi != nullptr) v = fmaf(sl2[e & 1], float(pb + t), v);
+            x[mt][e] = t < nv ? v : -INFINITY;
+          }
         }
       }
       // Running max and probabilities as in the 16-bit body; the rescale
@@ -914,22 +993,42 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           alpha[j] = ex2(m_run[j] - muse[j]);
           m_run[j] = mn;
         }
+        if (pair) alpha[1] = alpha[0];  // both columns hold head tig's sums
       }
       float ls0 = 0.f, ls1 = 0.f;
+      if (pair) {
 #pragma unroll
-      for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+        for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pr = ex2(x[mt][e] - muse[e & 1]);
-          if (e & 1)
-            ls1 += pr;
-          else
+          for (int r = 0; r < 2; ++r) {
+            const float pr = ex2(x[mt][2 * r] - muse[0]);
             ls0 += pr;
-          pw[(2 * tig + (e & 1)) * Cfg::kPRow + 16 * mt + gid + 8 * (e >> 1)] = pr;
+            pw[tig * Cfg::kPRow + 16 * mt + gid + 8 * r] = pr;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float pr = ex2(x[mt][e] - muse[e & 1]);
+            if (e & 1)
+              ls1 += pr;
+            else
+              ls0 += pr;
+            pw[(2 * tig + (e & 1)) * Cfg::kPRow + 16 * mt + gid + 8 * (e >> 1)] = pr;
+          }
         }
       }
-      l_run[0] = l_run[0] * alpha[0] + ls0;
-      l_run[1] = l_run[1] * alpha[1] + ls1;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float lsj = j ? ls1 : ls0;
+        const float lr = __fmul_rn(l_run[j], alpha[j]);
+        const float y = lsj - __fmul_rn(l_c[j], alpha[j]);
+        const float t = __fadd_rn(lr, y);
+        l_c[j] = __fsub_rn(__fsub_rn(t, lr), y);
+        l_run[j] = t;
+      }
       __syncwarp();
       // The chunk's value products accumulate from zero and join the running
       // sums with one fp32 FMA each (acc * alpha + chunk): the tensor core's
@@ -940,15 +1039,21 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       for (int dt = 0; dt < DT; ++dt) cacc[dt][0] = cacc[dt][1] = cacc[dt][2] = cacc[dt][3] = 0.f;
 #pragma unroll
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
-        // B fragments: head gid, tokens 16mt + 4tig + {0, 1} (k-step 0) and
-        // + {2, 3} (k-step 1).
-        const float4 pq = *reinterpret_cast<const float4 *>(pw + gid * Cfg::kPRow + 16 * mt +
+        // B fragments: column gid, tokens 16mt + 4tig + {0, 1} (k-step 0) and
+        // + {2, 3} (k-step 1); with column pairs ph holds column gid's term
+        // of head gid/2 (hi for even gid, lo for odd).
+        const int prow = pair ? (gid >> 1) : gid;
+        const float4 pq = *reinterpret_cast<const float4 *>(pw + prow * Cfg::kPRow + 16 * mt +
                                                             4 * tig);
         uint32_t ph[4], pl[4];
         split_tf32_fast(pq.x, ph[0], pl[0]);
         split_tf32_fast(pq.y, ph[1], pl[1]);
         split_tf32_fast(pq.z, ph[2], pl[2]);
         split_tf32_fast(pq.w, ph[3], pl[3]);
+        if (pair && (gid & 1)) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ph[e] = pl[e];
+        }
         const int tv = 16 * mt + 4 * tig;
         const float *vrow = reinterpret_cast<const float *>(vs + (tv / BS) * Cfg::kPageBytes) +
                             gid * BS + (tv % BS);
@@ -970,8 +1075,9 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
             const int o = 4 * k;
             mma_tf32_16808(cacc[dt], al[o], al[o + 1], al[o + 2], al[o + 3], ph[2 * k],
                            ph[2 * k + 1]);
-            mma_tf32_16808(cacc[dt], ah[o], ah[o + 1], ah[o + 2], ah[o + 3], pl[2 * k],
-                           pl[2 * k + 1]);
+            if (!pair)
+              mma_tf32_16808(cacc[dt], ah[o], ah[o + 1], ah[o + 2], ah[o + 3], pl[2 * k],
+                             pl[2 * k + 1]);
             mma_tf32_16808(cacc[dt], ah[o], ah[o + 1], ah[o + 2], ah[o + 3], ph[2 * k],
                            ph[2 * k + 1]);
           }
@@ -987,6 +1093,8 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     }
 
     // Full per-head sums: lanes sharing lane%4 hold the same two heads.
+    l_run[0] -= l_c[0];
+    l_run[1] -= l_c[1];
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l_run[0] += __shfl_xor_sync(FULL, l_run[0], o);
@@ -999,20 +1107,33 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
                           min(p.wait_limit_ns, uint64_t(100000000ull)));
       __syncwarp();
     }
+    if (pair) {
 #pragma unroll
-    for (int dt = 0; dt < DT; ++dt) {
+      for (int dt = 0; dt < DT; ++dt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = 16 * dt + gid + 8 * (e >> 1);
-        const int h = 2 * tig + (e & 1);
-        epi[h * D + d] = acc[dt][e];
+        for (int r = 0; r < 2; ++r)
+          epi[tig * D + 16 * dt + gid + 8 * r] = acc[dt][2 * r] + acc[dt][2 * r + 1];
       }
-    }
-    if (lane < 4) {
-      epi[kMaxGroup * D + 2 * lane] = m_run[0];
-      epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
-      epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
-      epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
+      if (lane < 4) {
+        epi[kMaxGroup * D + lane] = m_run[0];
+        epi[kMaxGroup * D + kMaxGroup + lane] = l_run[0];
+      }
+    } else {
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = 16 * dt + gid + 8 * (e >> 1);
+          const int h = 2 * tig + (e & 1);
+          epi[h * D + d] = acc[dt][e];
+        }
+      }
+      if (lane < 4) {
+        epi[kMaxGroup * D + 2 * lane] = m_run[0];
+        epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
+        epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
+        epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
+      }
     }
   }
 
