@@ -471,10 +471,11 @@ def oracle_metadata(inp, spec):
 
 
 def cpu_baseline(inp, spec, budget_s=10.0, threads=None):
-    """The oracle on a bounded sample: sequences in a seeded order until the
-    oracle has spent the time budget (after one untimed warm-up sequence);
-    returns KV-read GB/s over the sample, the threads it was given and the
-    process CPU time over its wall time (how many cores it kept busy)."""
+    """The oracle on a bounded sample: sequences in a seeded order (cycling
+    through the batch when it is smaller than the budget) until the oracle has
+    spent the time budget, after one untimed warm-up sequence; returns KV-read
+    GB/s over the sample, the threads it was given and the process CPU time
+    over its wall time (how many cores it kept busy)."""
     prev = torch.get_num_threads()
     cores = cpu_threads(threads)
     try:
@@ -486,23 +487,28 @@ def cpu_baseline(inp, spec, budget_s=10.0, threads=None):
         spent = time.perf_counter() - t0
         cpu = time.process_time() - c0
         oracle_step(inp, spec, [order[-1]], splits)  # warm-up, not counted
-        done, nbytes = [], 0
-        for s in order:
+        steps, nbytes, distinct = 0, 0, set()
+        while True:
+            s = order[steps % len(order)]
             nb, dt, dc = oracle_step(inp, spec, [s], splits)
             nbytes += nb
             spent += dt
             cpu += dc
-            done.append(s)
+            steps += 1
+            distinct.add(s)
             if spent >= budget_s:
                 break
     finally:
         torch.set_num_threads(prev)
+    n = len(inp["seq_lens_list"])
+    what = (f"{steps} of {n} sequences" if steps <= n else
+            f"{steps} sequence decodes cycling through all {n} sequences")
     return {"value": nbytes / spent / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "wall_s": round(spent, 3), "cpu_time_s": round(cpu, 3),
+            "wall_s": round(spent, 6), "cpu_time_s": round(cpu, 6),
             "cpu_time_over_wall": round(cpu / spent, 2),
-            "sample": (f"{len(done)} of {len(inp['seq_lens_list'])} sequences "
-                       f"({nbytes / 1e9:.3f} GB of K/V) of {spec.name} plus the whole batch's "
-                       f"metadata, float64, {spent:.1f} s of oracle time on {cores} thread(s)")}
+            "sample": (f"{what} ({nbytes / 1e9:.3f} GB of K/V) of {spec.name} plus the whole "
+                       f"batch's metadata, float64, {spent:.1f} s of oracle time on {cores} "
+                       f"thread(s)")}
 
 
 # ------------------------------------------------------------------ arms --
