@@ -150,7 +150,9 @@ constexpr int resident_ctas() {
   return 0;
 }
 
-template <typename T, typename KV, int D, int BS, int WARPS>
+// PAIR (fp32 and fp8 caches, groups of at most 4 query heads): the MMA
+// columns carry two terms per head (see the fp8 and fp32 bodies).
+template <typename T, typename KV, int D, int BS, int WARPS, bool PAIR>
 __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     paged_attention_kernel(const AttnParams p) {
   using Cfg = AttnCfg<KV, D, BS, WARPS>;
@@ -540,7 +542,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     // value product columns 2h and 2h + 1 carry the hi and lo parts of head
     // h's probabilities, so one MMA does what the hi and lo MMAs do otherwise.
     // A lane then holds one head (tig) instead of two.
-    const bool pair = g <= 4;
+    constexpr bool pair = PAIR;
     // Query fragments (B operand, f16) of column gid: dims 16ks + 4tig + {0, 1}
     // on k-slots 2tig, 2tig+1 and dims 16ks + 4tig + {2, 3} on 2tig+8, 2tig+9.
     uint32_t qf[DT][2];
@@ -852,7 +854,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     constexpr int DK = D / 8;   // 8-dim k-steps of the key product
     constexpr int DT = D / 16;  // 16-dim tiles of the value product
     const int gid = lane >> 2, tig = lane & 3;
-    const bool pair = g <= 4;
+    constexpr bool pair = PAIR;
     // Query fragments (B operand): column gid, dims 8kk + tig and 8kk + tig + 4;
     // with column pairs qh holds column gid's term (hi of head gid/2 for even
     // gid, lo for odd) and ql is not used.

@@ -47,16 +47,32 @@ bool ensure_smem_attr(Kernel kernel, int bytes, std::atomic<unsigned long long> 
   return true;
 }
 
-template <typename T, typename KV, int D, int BS, int W>
-pkv_status_t launch_instance(const AttnParams &p, dim3 grid, cudaStream_t stream) {
+template <typename T, typename KV, int D, int BS, int W, bool PAIR>
+pkv_status_t launch_kernel(const AttnParams &p, dim3 grid, cudaStream_t stream) {
   using Cfg = AttnCfg<KV, D, BS, W>;
   static std::atomic<unsigned long long> done{0};
-  auto kernel = paged_attention_kernel<T, KV, D, BS, W>;
+  auto kernel = paged_attention_kernel<T, KV, D, BS, W, PAIR>;
   if (!ensure_smem_attr(kernel, Cfg::kSmemBytes, done)) return PKV_ERR_CUDA;
   return launch_programmatic(kernel, grid, dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) ==
                  cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
+}
+
+// The fp32 and fp8 bodies have a column-pair form for groups of at most 4
+// query heads (every CTA then serves the whole group), compiled as its own
+// kernel: one kernel holding both forms ran the other form 4 % slower.
+template <typename T, typename KV>
+constexpr bool has_column_pairs() {
+  return std::is_same<T, float>::value || is_fp8<KV>::value;
+}
+
+template <typename T, typename KV, int D, int BS, int W>
+pkv_status_t launch_instance(const AttnParams &p, dim3 grid, cudaStream_t stream) {
+  if constexpr (has_column_pairs<T, KV>()) {
+    if (p.group <= 4) return launch_kernel<T, KV, D, BS, W, true>(p, grid, stream);
+  }
+  return launch_kernel<T, KV, D, BS, W, false>(p, grid, stream);
 }
 
 // Instances are built for WARPS in {1, 2, 4}; a 4-warp instance only when its
