@@ -150,8 +150,8 @@ constexpr int resident_ctas() {
   return 0;
 }
 
-// PAIR (fp32 and fp8 caches, groups of at most 4 query heads): the MMA
-// columns carry two terms per head (see the fp8 and fp32 bodies).
+// PAIR (groups of at most 4 query heads): the MMA columns carry two terms
+// per head, so one MMA does the work of two (see each body).
 template <typename T, typename KV, int D, int BS, int WARPS, bool PAIR>
 __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
     paged_attention_kernel(const AttnParams p) {
@@ -337,12 +337,17 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
 
   if constexpr (kMma) {
     constexpr int DT = D / 16;  // 16-dim tiles
-    // Q^T fragments (B operand): dims 16ks + 2(lane%4) (+1), (+8); head lane/4.
+    // Column pairs (groups of at most 4 heads): head h takes column 2h of the
+    // score product (column 2h + 1 has a zero query) and columns 2h, 2h + 1
+    // of the value product carry the hi and lo parts of its probabilities, so
+    // one MMA does the work of the hi and lo MMAs; a lane holds head lane%4.
+    constexpr bool pair = PAIR;
+    // Q^T fragments (B operand): dims 16ks + 2(lane%4) (+1), (+8); column lane/4.
     uint32_t qf[DT][2];
     {
-      const int h = lane >> 2;
+      const int h = pair ? (((lane >> 2) & 1) ? kMaxGroup : (lane >> 3)) : (lane >> 2);
       const uint16_t *qb = static_cast<const uint16_t *>(p.q) + int64_t(seq) * p.q_s0 +
-                           int64_t(h0 + h) * p.q_s1;
+                           int64_t(h0 + min(h, g - 1)) * p.q_s1;
 #pragma unroll
       for (int ks = 0; ks < DT; ++ks) {
 #pragma unroll
@@ -358,12 +363,12 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       }
     }
     // ALiBi slopes (log2 units) of this lane's two score columns: heads
-    // 2*(lane%4) and 2*(lane%4)+1 of the CTA.
+    // 2*(lane%4) and 2*(lane%4)+1 of the CTA (with column pairs: head lane%4).
     float sl2[2] = {0.f, 0.f};
     if (p.alibi != nullptr) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int h = 2 * (lane & 3) + j;
+        const int h = pair ? (j ? kMaxGroup : (lane & 3)) : 2 * (lane & 3) + j;
         if (h < g) sl2[j] = p.alibi[h0 + h] * kLog2e;
       }
     }
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           const int t = 16 * mt + (lane >> 2) + 8 * (e >> 1);
           float v = (s0[e] + s1[e]) * p.scale_log2;
           if (p.alibi != nullptr) v = fmaf(sl2[e & 1], float(pb + t), v);
-          x[mt][e] = t < nv ? v : -INFINITY;
+          x[mt][e] = (t < nv && !(pair && (e & 1))) ? v : -INFINITY;
         }
       }
       // The running max moves only where some lane's score exceeds it: then
@@ -456,6 +461,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           alpha[j] = ex2(m_run[j] - muse[j]);
           m_run[j] = mn;
         }
+        if (pair) alpha[1] = alpha[0];  // both columns hold head lane%4's sums
         if (__any_sync(FULL, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
           for (int dt = 0; dt < DT; ++dt) {
@@ -470,7 +476,8 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
 #pragma unroll
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pr[mt][e] = ex2(x[mt][e] - muse[e & 1]);
+        for (int e = 0; e < 4; ++e)
+          pr[mt][e] = (pair && (e & 1)) ? 0.f : ex2(x[mt][e] - muse[e & 1]);
       }
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
@@ -482,13 +489,24 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       l_run[1] = l_run[1] * alpha[1] + ls1;
 #pragma unroll
       for (int mt = 0; mt < Cfg::kMTiles; ++mt) {
-        const uint32_t hi0 = pack2<T>(pr[mt][0], pr[mt][1]);
-        const uint32_t hi1 = pack2<T>(pr[mt][2], pr[mt][3]);
-        const float2 f0 = unpack2<T>(hi0), f1 = unpack2<T>(hi1);
-        const uint32_t lo0 = pack2<T>(pr[mt][0] - f0.x, pr[mt][1] - f0.y);
-        const uint32_t lo1 = pack2<T>(pr[mt][2] - f1.x, pr[mt][3] - f1.y);
-        const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
-        const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
+        uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+        if (pair) {
+          // Columns 2(lane%4), 2(lane%4)+1: head lane%4's hi and lo parts.
+          const float2 f0 = unpack2<T>(pack2<T>(pr[mt][0], 0.f));
+          const float2 f1 = unpack2<T>(pack2<T>(pr[mt][2], 0.f));
+          bh0 = movmatrix_trans(pack2<T>(pr[mt][0], pr[mt][0] - f0.x));
+          bh1 = movmatrix_trans(pack2<T>(pr[mt][2], pr[mt][2] - f1.x));
+        } else {
+          const uint32_t hi0 = pack2<T>(pr[mt][0], pr[mt][1]);
+          const uint32_t hi1 = pack2<T>(pr[mt][2], pr[mt][3]);
+          const float2 f0 = unpack2<T>(hi0), f1 = unpack2<T>(hi1);
+          const uint32_t lo0 = pack2<T>(pr[mt][0] - f0.x, pr[mt][1] - f0.y);
+          const uint32_t lo1 = pack2<T>(pr[mt][2] - f1.x, pr[mt][3] - f1.y);
+          bh0 = movmatrix_trans(hi0);
+          bh1 = movmatrix_trans(hi1);
+          bl0 = movmatrix_trans(lo0);
+          bl1 = movmatrix_trans(lo1);
+        }
         const int tok0 = 16 * mt + 8 * (jm >> 1);
         const uint32_t rowv = vs_a + (tok0 / BS) * Cfg::kPageBytes + (tok0 % BS) * 2 +
                               (rr + 8 * (jm & 1)) * (BS * 2);
@@ -497,7 +515,7 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
           uint32_t a[4];
           ldsm_x4(rowv + dt * (16 * BS * 2), a[0], a[1], a[2], a[3]);
           Mma16816<T>::run(acc[dt], a, bh0, bh1);
-          Mma16816<T>::run(acc[dt], a, bl0, bl1);
+          if (!pair) Mma16816<T>::run(acc[dt], a, bl0, bl1);
         }
       }
       __syncwarp();
@@ -518,20 +536,33 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
       __syncwarp();
     }
     // Stage memory of this warp is free now: store O (as [head][dim]), m, l.
+    if (pair) {
 #pragma unroll
-    for (int dt = 0; dt < DT; ++dt) {
+      for (int dt = 0; dt < DT; ++dt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = 16 * dt + (lane >> 2) + 8 * (e >> 1);
-        const int h = 2 * (lane & 3) + (e & 1);
-        epi[h * D + d] = acc[dt][e];
+        for (int r = 0; r < 2; ++r)
+          epi[(lane & 3) * D + 16 * dt + (lane >> 2) + 8 * r] = acc[dt][2 * r] + acc[dt][2 * r + 1];
       }
-    }
-    if (lane < 4) {
-      epi[kMaxGroup * D + 2 * lane] = m_run[0];
-      epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
-      epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
-      epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
+      if (lane < 4) {
+        epi[kMaxGroup * D + lane] = m_run[0];
+        epi[kMaxGroup * D + kMaxGroup + lane] = l_run[0];
+      }
+    } else {
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = 16 * dt + (lane >> 2) + 8 * (e >> 1);
+          const int h = 2 * (lane & 3) + (e & 1);
+          epi[h * D + d] = acc[dt][e];
+        }
+      }
+      if (lane < 4) {
+        epi[kMaxGroup * D + 2 * lane] = m_run[0];
+        epi[kMaxGroup * D + 2 * lane + 1] = m_run[1];
+        epi[kMaxGroup * D + kMaxGroup + 2 * lane] = l_run[0];
+        epi[kMaxGroup * D + kMaxGroup + 2 * lane + 1] = l_run[1];
+      }
     }
   } else if constexpr (kFp8) {
     // ------------------------------------- fp8 cache, f16 tensor-core body --

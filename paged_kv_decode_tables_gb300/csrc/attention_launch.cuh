@@ -59,19 +59,12 @@ pkv_status_t launch_kernel(const AttnParams &p, dim3 grid, cudaStream_t stream) 
              : PKV_ERR_CUDA;
 }
 
-// The fp32 and fp8 bodies have a column-pair form for groups of at most 4
-// query heads (every CTA then serves the whole group), compiled as its own
-// kernel: one kernel holding both forms ran the other form 4 % slower.
-template <typename T, typename KV>
-constexpr bool has_column_pairs() {
-  return std::is_same<T, float>::value || is_fp8<KV>::value;
-}
-
+// Every body has a column-pair form for groups of at most 4 query heads
+// (every CTA then serves the whole group), compiled as its own kernel: one
+// kernel holding both forms ran the other form 4 % slower.
 template <typename T, typename KV, int D, int BS, int W>
 pkv_status_t launch_instance(const AttnParams &p, dim3 grid, cudaStream_t stream) {
-  if constexpr (has_column_pairs<T, KV>()) {
-    if (p.group <= 4) return launch_kernel<T, KV, D, BS, W, true>(p, grid, stream);
-  }
+  if (p.group <= 4) return launch_kernel<T, KV, D, BS, W, true>(p, grid, stream);
   return launch_kernel<T, KV, D, BS, W, false>(p, grid, stream);
 }
 
