@@ -118,8 +118,12 @@ struct AttnCfg {
   static constexpr int kStageBytes = 2 * kHalfStage;
   // Two stages per warp: measured, more resident warps beat deeper per-warp
   // rings at every head size (a 16 KiB ring of 4 KiB stages at head size 64
-  // loses 2-25 % to two stages).
-  static constexpr int kStages = 2;
+  // loses 2-25 % to two stages).  One exception, also measured: one-byte
+  // caches with two warps per CTA (16-token chunks of 4 KiB at head size 128)
+  // take three stages, whose second chunk of look-ahead covers the copy
+  // latency that the shorter column-pair chunk no longer hides (ragged batch
+  // 309 -> 305 us; one warp with 32-token chunks loses 4 % with three).
+  static constexpr int kStages = (kElem == 1 && D <= 128 && WARPS == 2) ? 3 : 2;
   static constexpr int kWarpBytes = kStages * kStageBytes;
   static constexpr int kEpiFloats = kMaxGroup * D + 2 * kMaxGroup;
   // fp32 caches: per-warp probabilities of one chunk, [head][token] with rows

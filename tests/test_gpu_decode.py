@@ -335,6 +335,44 @@ def test_copy_wait_timeout_is_reported_and_the_context_survives():
         assert_attention_close(out, _oracle_v1(inp), DT[dtype], f"after timeout {dtype}")
 
 
+@pytest.mark.parametrize("dtype,kv,alibi", [("f32", "auto", False), ("bf16", "auto", True),
+                                             ("f16", "fp8_e4m3", False), ("bf16", "fp8_e5m2", True)])
+def test_column_pair_and_full_forms_agree(dtype, kv, alibi):
+    """A group of 4 query heads runs the column-pair kernel, a group of 8 the
+    full one: the same 4 queries duplicated into a group of 8 must give the
+    same outputs and partials for heads 0-3 up to rounding (one ulp of the
+    output type; fp32 4e-6)."""
+    lens = [1000, 37, 2500, 1]
+    inp = _inputs(dtype, 128, 16, 8, 2, lens, seed=31, kv_cache_dtype=kv, k_scale=0.5,
+                  v_scale=2.0, alibi=alibi)
+    g4 = on_device(inp)
+    sel = torch.tensor([k * 8 + j for k in range(2) for j in range(4)], device="cuda")
+    src = torch.tensor([k * 4 + j % 4 for k in range(2) for j in range(8)], device="cuda")
+    g8 = dict(g4)
+    g8["query"] = g4["query"].index_select(1, src).contiguous()
+    g8["num_heads"] = 16
+    if alibi:
+        g8["alibi_slopes"] = g4["alibi_slopes"].index_select(0, src).contiguous()
+    o4 = run_v1(g4).double()
+    o8 = run_v1(g8).index_select(1, sel).double()
+    if dtype == "f32":
+        tol = torch.full_like(o4, 4e-6)
+    else:
+        m = {"f16": 10, "bf16": 7}[dtype]
+        tol = torch.pow(2.0, torch.floor(torch.log2(o4.abs().clamp_min(1e-30))) - m) + 1e-6
+    diff = (o4 - o8).abs()
+    assert bool((diff <= tol).all()), f"{dtype}/{kv}: max diff {float(diff.max()):.3e}"
+    maxP = -(-inp["max_blocks_per_seq"] * 16 // 512)
+    t4, e4, m4, _ = run_v2(g4, maxP, partition_size=512)
+    t8, e8, m8, _ = run_v2(g8, maxP, partition_size=512)
+    t8, e8, m8 = (x.index_select(1, sel) for x in (t8, e8, m8))
+    live = e4 > 0
+    assert torch.equal(live, e8 > 0)
+    assert bool(((t4 - t8).abs()[live] <= 1e-5 * (1 + t4.abs()[live])).all())
+    assert bool(((e4 - e8).abs()[live] <= 1e-5 * e4.abs()[live]).all())
+    assert bool(((m4 - m8).abs()[live] <= 1e-5 * (1 + m4.abs()[live])).all())
+
+
 @pytest.mark.parametrize("dtype,D,bs,H,Hk", [("bf16", 128, 16, 16, 1), ("bf16", 128, 16, 128, 8),
                                              ("f16", 64, 8, 18, 2), ("bf16", 256, 32, 64, 2),
                                              ("f32", 64, 16, 32, 1), ("bf16", 128, 16, 64, 1)])
