@@ -9,9 +9,10 @@
 //
 // Data movement.  A (block, kv_head) page of either cache is one contiguous
 // run of head_size*block_size elements (4 KiB at bf16/128/16).  Each warp runs
-// its own two-stage pipeline: its lane 0 issues cp.async.bulk copies of whole
-// K and V pages into the warp's shared-memory stages, tracked by one mbarrier
-// per stage, and the warp computes on one stage while the other is in flight.
+// its own pipeline of two stages (three in one instance family, see AttnCfg):
+// its lane 0 issues cp.async.bulk copies of whole K and V pages into the
+// warp's shared-memory stages, tracked by one mbarrier per stage, and the warp
+// computes on one stage while the next ones are in flight.
 // Warp w of the CTA takes chunks w, w+WARPS, ... of the partition's tokens (a
 // chunk is 16 tokens, 32 for one-byte caches in some instances, or one page,
 // whichever is larger).
