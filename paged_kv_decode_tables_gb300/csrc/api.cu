@@ -17,6 +17,7 @@ using pkv::AttnParams;
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_per_sm[kMaxDevices];
 std::atomic<int> g_forced_warps{0};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<unsigned> g_extra_expect_tx{0};
@@ -30,6 +31,19 @@ int sm_count() {
   if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
     v = 148;
   g_sm_count[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Shared memory of one SM in bytes (228 KiB on GB300 when the query fails).
+int smem_per_sm() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 233472;
+  int v = g_smem_per_sm[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      v <= 0)
+    v = 233472;
+  g_smem_per_sm[dev].store(v, std::memory_order_relaxed);
   return v;
 }
 
@@ -159,7 +173,10 @@ AttnParams make_params(const pkv_decode_args_t *a) {
 // - split-KV with few units: 4;
 // - fp32 caches: at most 2 (a warp's two 16-token stages take 32 KiB at head
 //   size 128, so 4-warp CTAs leave one CTA and 4 warps per SM: the fp32 GQA
-//   single pass ran 0.60 of the copy bandwidth on 4 warps, 0.90 on 2).
+//   single pass ran 0.60 of the copy bandwidth on 4 warps, 0.90 on 2);
+// - 2 instead of 4 whenever fewer than three 4-warp CTAs fit in an SM's shared
+//   memory (16-bit caches at head size 256: the GQA single pass ran 0.91 of
+//   the copy bandwidth on 4 warps, 0.975 on 2).
 enum class Pass { kSingle, kFixed, kSplits };
 
 int pick_warps(const pkv_decode_args_t *a, int64_t units, Pass pass, int partition_size) {
@@ -176,6 +193,11 @@ int pick_warps(const pkv_decode_args_t *a, int64_t units, Pass pass, int partiti
   else
     want = 2;
   if (a->dtype == PKV_F32 && want > 2) want = 2;
+  if (want == 4) {
+    // 1 KiB per CTA is reserved by the system.
+    const size_t s4 = smem_for(a->dtype, a->kv_cache_dtype, a->head_size, a->block_size, 4);
+    if (s4 != 0 && (s4 + 1024) * 3 > size_t(smem_per_sm())) want = 2;
+  }
   while (want > 1 && !have(want)) want /= 2;
   return want;
 }
