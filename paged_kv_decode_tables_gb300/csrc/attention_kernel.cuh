@@ -120,11 +120,13 @@ struct AttnCfg {
   // Two stages per warp: measured, more resident warps beat deeper per-warp
   // rings at every head size (a 16 KiB ring of 4 KiB stages at head size 64
   // loses 2-25 % to two stages).  One exception, also measured: one-byte
-  // caches with two warps per CTA (16-token chunks of 4 KiB at head size 128)
-  // take three stages, whose second chunk of look-ahead covers the copy
-  // latency that the shorter column-pair chunk no longer hides (ragged batch
-  // 309 -> 305 us; one warp with 32-token chunks loses 4 % with three).
-  static constexpr int kStages = (kElem == 1 && D <= 128 && WARPS == 2) ? 3 : 2;
+  // caches with two warps per CTA and 16-token pages (a chunk is one page:
+  // 4 KiB at head size 128) take three stages, whose second chunk of
+  // look-ahead covers the copy latency that the shorter column-pair chunk no
+  // longer hides (ragged batch 309 -> 305 us).  With 32-token pages three
+  // 8 KiB stages cost residency (ragged batch 312 -> 388 us), and one warp
+  // with 32-token chunks loses 4 % with three.
+  static constexpr int kStages = (kElem == 1 && D <= 128 && WARPS == 2 && BS == 16) ? 3 : 2;
   static constexpr int kWarpBytes = kStages * kStageBytes;
   static constexpr int kEpiFloats = kMaxGroup * D + 2 * kMaxGroup;
   // fp32 caches: per-warp probabilities of one chunk, [head][token] with rows
