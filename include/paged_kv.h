@@ -25,7 +25,14 @@
  *   (a caller-zeroed device int32, may be NULL) and carries on; results that
  *   depend on the bad value are then unspecified.
  * - Arithmetic: fp32 accumulation for every input dtype; softmax statistics and
- *   split-KV partials are fp32.
+ *   split-KV partials are fp32.  Products: fp16/bf16 operands are exact in
+ *   fp32; fp8 codes are widened exactly to f16 (a bf16 query is scaled by a
+ *   power of two into f16's range without rounding); the probabilities enter
+ *   the value product as a hi + lo pair of 16-bit values.  fp32 operands are
+ *   split into two tf32 terms each, and a product takes three of the four term
+ *   pairs (all four when a kv head serves at most 4 query heads), about 2^-21
+ *   relative per product; the fp32 output stays within 1e-5 of the exact
+ *   result on the tested inputs.
  *
  * Cache layouts (vLLM's, as restated on the page "paged_attention_v2_triton.py",
  * argument comments of _paged_attn_v2_partition_kernel):
