@@ -196,7 +196,8 @@ class DecodeStep:
     """Device buffers of one workload and the launches of one step, issued
     straight through the C ABI with argument structs prepared once."""
 
-    def __init__(self, name: str, seed: int, device, num_seqs=None, fused_metadata=True):
+    def __init__(self, name: str, seed: int, device, num_seqs=None, fused_metadata=True,
+                 lpt=False):
         import ctypes
 
         import paged_kv_decode_tables_gb300 as pkv
@@ -254,6 +255,13 @@ class DecodeStep:
         self.fused_metadata = fused_metadata
         self.launches_per_step = {"v1": 1, "v2_fixed": 2,
                                   "v2_splits": 3 if fused_metadata else 4}[self.mode]
+        # Single pass, longest sequence first: each step orders the batch on
+        # the device (pkv_order_by_length) and the decode launches in that order.
+        self.lpt = lpt and self.mode == "v1"
+        if self.lpt:
+            self.order = torch.empty(B, dtype=torch.int32, device=dev)
+            self.args.seq_order = self.order.data_ptr()
+            self.launches_per_step += 1
         # Algorithmic bytes of one launch of the attention kernel: K+V of every
         # token, the queries, the block ids and lengths it reads, and (single
         # pass) its output.  The fp32 split-KV partials are counted apart.
@@ -283,6 +291,11 @@ class DecodeStep:
                     (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
                 mark(name, 0)
 
+        if self.lpt:
+            begin("pkv_order_by_length")
+            self._check(lib.pkv_order_by_length(self.order.data_ptr(), self.inp["seq_lens"].data_ptr(),
+                                                self.B, s), "order")
+            mark("pkv_order_by_length", 1)
         if self.mode == "v2_splits" and self.fused_metadata:
             inp = self.inp
             bt = inp["block_tables"]
@@ -771,7 +784,7 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     step = DecodeStep(args.workload, seed=rank, device="cuda", num_seqs=args.num_seqs,
-                      fused_metadata=args.metadata == "fused")
+                      fused_metadata=args.metadata == "fused", lpt=args.lpt)
     if args.warps:
         step.pkv.set_attention_warps(args.warps)
     if args.fp8_kernel == "tensor-memory":
@@ -845,6 +858,7 @@ def run_ours(args):
         "metadata": (("one launch (prepare_decode_metadata)" if step.fused_metadata else
                       "copy_page_indices + compute_num_kv_splits")
                      if step.mode == "v2_splits" else None),
+        "launch_order": "longest first (pkv_order_by_length in the step)" if step.lpt else "sequence order",
         "roofline": roofline,
         "step_share": {"attention_kernel": round(roofline["avg_launch_us"] / 1e3 / ms_step, 4)},
         "kernel_us": kernel_us,
@@ -1072,6 +1086,8 @@ def main(argv=None):
                     help="kernel for fp8 caches of head size 128 / block size 16")
     ap.add_argument("--metadata", choices=["fused", "separate"], default="fused",
                     help="ragged step: metadata in one launch or the two separate kernels")
+    ap.add_argument("--lpt", action="store_true",
+                    help="single pass: order the batch longest first on the device each step")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time stream launches instead of CUDA-graph replays of the step")
     ap.add_argument("--no-clocks", action="store_true")

@@ -88,6 +88,7 @@ typedef enum {
 #define PKV_ERRF_SPLITS 4u   /* num_kv_splits[s] outside [1, max_num_partitions]: clamped */
 #define PKV_ERRF_INDPTR 8u   /* indptr row negative, longer than the table, or past the output */
 #define PKV_ERRF_TIMEOUT 16u /* a wait for a copy into shared memory exceeded its time limit */
+#define PKV_ERRF_ORDER 32u   /* seq_order entry outside [0, num_seqs): the identity was used */
 
 /*
  * Inputs shared by paged_attention_decode and paged_attention_v2_partition.
@@ -118,6 +119,13 @@ typedef enum {
  *       al.) with the decode query at position seq_len - 1, the reading of the
  *       alibi_slopes argument the page "paged_attention_v2_triton.py" names.
  *       It enters max_logits of the split-KV pass like any logit.
+ *   seq_order: optional [num_seqs] int32 device array, a permutation of
+ *       0..num_seqs-1 (NULL: identity).  paged_attention_decode launches the
+ *       units of sequence seq_order[z] in the z-th place of its grid, e.g.
+ *       longest first from pkv_order_by_length; results do not depend on it.
+ *       An entry outside 0..num_seqs-1 is replaced by z and sets
+ *       PKV_ERRF_ORDER; duplicate entries leave sequences unprocessed.  The
+ *       split-KV entry points and the tensor-memory fp8 kernel ignore it.
  */
 typedef struct {
   int32_t num_seqs;
@@ -145,6 +153,7 @@ typedef struct {
   float k_scale;
   float v_scale;
   const float *alibi_slopes;
+  const int32_t *seq_order;
 } pkv_decode_args_t;
 
 /* Library version string, e.g. "paged_kv 0.2.0 sm_103a". */
@@ -468,6 +477,21 @@ pkv_status_t paged_attention_v2_noalloc(void *out, const int64_t out_stride[3],
                                         const pkv_decode_args_t *args, pkv_stream_t stream);
 /* Size in bytes of paged_attention_v2_noalloc's fixed scratch array. */
 size_t pkv_noalloc_scratch_bytes(void);
+
+/*
+ * Launch order for paged_attention_decode's seq_order, longest sequence first:
+ * a single pass starts one CTA per (sequence, kv head group) in grid order, so
+ * starting the longest units first shortens the grid's tail (longest
+ * processing time first).  One CTA sorts the lengths into 256 buckets by
+ * (max_len - len) * 256 / (max_len + 1); within a bucket the order is
+ * unspecified.  Negative lengths count as 0.
+ *   order:    [num_seqs] int32 device output, a permutation of 0..num_seqs-1.
+ *   seq_lens: [num_seqs] int32 device input.
+ * No host sync; PKV_ERR_INVALID_ARG for num_seqs < 0 or NULL pointers (with
+ * num_seqs > 0).
+ */
+pkv_status_t pkv_order_by_length(int32_t *order, const int32_t *seq_lens, int32_t num_seqs,
+                                 pkv_stream_t stream);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -20,6 +20,7 @@ __all__ = [
     "PKV_ERRF_SPLITS",
     "PKV_ERRF_INDPTR",
     "PKV_ERRF_TIMEOUT",
+    "PKV_ERRF_ORDER",
     "lib",
     "lib_path",
     "version",
@@ -36,6 +37,7 @@ __all__ = [
     "prepare_swa_spec_page_table",
     "paged_attention_v2_noalloc",
     "noalloc_scratch_bytes",
+    "order_by_length",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -45,6 +47,7 @@ PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA = 0, 1, 2, 3
 PKV_ERR_SCRATCH_TOO_SMALL = 4
 PKV_ERRF_BLOCK_ID, PKV_ERRF_SEQ_LEN, PKV_ERRF_SPLITS, PKV_ERRF_INDPTR, PKV_ERRF_TIMEOUT = (
     1, 2, 4, 8, 16)
+PKV_ERRF_ORDER = 32
 
 _DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
@@ -71,7 +74,7 @@ class DecodeArgs(ctypes.Structure):
         ("block_tables", _c_p), ("bt_stride", _c_i64 * 2),
         ("kv_indptr", _c_p), ("seq_lens", _c_p), ("err_flag", _c_p),
         ("kv_cache_dtype", _c_i32), ("k_scale", _c_f32), ("v_scale", _c_f32),
-        ("alibi_slopes", _c_p),
+        ("alibi_slopes", _c_p), ("seq_order", _c_p),
     ]
 
 
@@ -153,6 +156,8 @@ def lib() -> ctypes.CDLL:
     L.copy_page_indices.restype = ctypes.c_int
     L.copy_page_indices.argtypes = [_c_p, _c_i64, _c_p, _c_i32, _c_i64, _c_i64, _c_p, _c_i32,
                                     _c_p, _c_p]
+    L.pkv_order_by_length.restype = ctypes.c_int
+    L.pkv_order_by_length.argtypes = [_c_p, _c_p, _c_i32, _c_p]
     L.compute_num_kv_splits.restype = ctypes.c_int
     L.compute_num_kv_splits.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                         _c_i32, _c_p]
@@ -321,22 +326,42 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
                            max_blocks_per_seq: Optional[int] = None,
                            kv_cache_dtype: str = "auto", k_scale: float = 1.0,
                            v_scale: float = 1.0, alibi_slopes: Optional[torch.Tensor] = None,
-                           stream=None) -> None:
+                           seq_order: Optional[torch.Tensor] = None, stream=None) -> None:
     """Single-pass decode into ``out [num_seqs, num_heads, head_size]`` (query's dtype).
 
     ``kv_cache_dtype`` ("auto", "fp8", "fp8_e4m3", "fp8_e5m2") with uint8 code
     caches, or float8 caches under "auto", selects an fp8 cache dequantised as
     ``code * k_scale`` / ``code * v_scale``; ``alibi_slopes`` (float32
-    ``[num_heads]``) adds ``slope_h * (t - seq_len + 1)`` to the logits."""
+    ``[num_heads]``) adds ``slope_h * (t - seq_len + 1)`` to the logits;
+    ``seq_order`` (int32 ``[num_seqs]``, a permutation, e.g. from
+    :func:`order_by_length`) sets the order in which sequences are launched."""
     _cuda(out, "out")
     if out.dtype != query.dtype or tuple(out.shape) != tuple(query.shape):
         raise ValueError("out must match query's shape and dtype")
     a = _decode_args(query, key_cache, value_cache, block_tables, seq_lens, scale, kv_indptr,
                      err_flag, max_blocks_per_seq, kv_cache_dtype, k_scale,
                      v_scale, alibi_slopes)
+    if seq_order is not None:
+        _cuda(seq_order, "seq_order")
+        if (seq_order.dtype != torch.int32 or not seq_order.is_contiguous() or
+                tuple(seq_order.shape) != (query.shape[0],)):
+            raise ValueError("seq_order must be a contiguous int32 [num_seqs] tensor")
+        a.seq_order = _ptr(seq_order)
     os_ = _I64x3(*out.stride())
     _check(lib().paged_attention_decode(_ptr(out), os_, ctypes.byref(a), _stream(stream)),
            "paged_attention_decode")
+
+
+def order_by_length(order: torch.Tensor, seq_lens: torch.Tensor, stream=None) -> None:
+    """Longest-first launch order of ``seq_lens`` into ``order`` (int32, same length)."""
+    for t, n in ((order, "order"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.dim() != 1:
+            raise ValueError(f"{n} must be a contiguous 1-D int32 tensor")
+    if order.numel() != seq_lens.numel():
+        raise ValueError("order and seq_lens must have the same length")
+    _check(lib().pkv_order_by_length(_ptr(order), _ptr(seq_lens), order.numel(), _stream(stream)),
+           "pkv_order_by_length")
 
 
 def paged_attention_v2_partition(tmp_out: torch.Tensor, exp_sums: torch.Tensor,

@@ -157,6 +157,7 @@ AttnParams make_params(const pkv_decode_args_t *a) {
   p.scale_log2 = (fp8 ? a->scale * a->k_scale : a->scale) * 1.44269504088896340736f;
   p.out_scale = fp8 ? a->v_scale : 1.0f;
   p.alibi = a->alibi_slopes;
+  p.order = nullptr;  // set by paged_attention_decode only
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   // The test hook is one-shot: the launch that reads it clears it, so a hook
   // left set can delay at most one launch, never every later one.
@@ -269,6 +270,7 @@ pkv_status_t paged_attention_decode(void *out, const int64_t out_stride[3],
   p.o_s1 = out_stride[1];
   p.o_s2 = out_stride[2];
   p.max_parts = 1;
+  p.order = args->seq_order;
   dim3 grid(1, args->num_kv_heads * p.head_groups, args->num_seqs);
   if (use_tensor_memory_kernel(args))
     return pkv::launch_attention_fp8_tc(args, p, grid, reinterpret_cast<cudaStream_t>(stream));

@@ -90,6 +90,7 @@ struct AttnParams {
   uint32_t extra_expect_tx;  // test hook: bytes a stage expects that never arrive (0)
   const float *alibi;        // [num_heads] ALiBi slopes, or null
   float out_scale;           // multiplies the normalised output (v_scale for fp8 caches, else 1)
+  const int32_t *order;      // single pass: grid z -> sequence (a permutation), or null
 };
 
 constexpr int kMaxGroup = 8;
@@ -178,13 +179,23 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
   const int part = blockIdx.x;
   const int kvh = int(blockIdx.y) / p.head_groups;
   const int hsub = int(blockIdx.y) - kvh * p.head_groups;
-  const int seq = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = min(kMaxGroup, p.group - hsub * kMaxGroup);  // query heads of this CTA
   const bool leader = threadIdx.x == 0;
   grid_dependency_wait();
   allow_dependent_launch();
+  int seq = blockIdx.z;
+  if (p.order != nullptr) {
+    // Caller-given launch order (e.g. longest first); an entry out of range
+    // falls back to the identity and is flagged.
+    const int s = p.order[blockIdx.z];
+    if (s >= 0 && s < int(gridDim.z)) {
+      seq = s;
+    } else if (leader) {
+      flag_error(p.err, 32u);
+    }
+  }
 
   // ---------------------------------------------------- work decomposition --
   int L = p.seq_lens[seq];

@@ -10,7 +10,7 @@ import oracle
 import paged_kv_decode_tables_gb300 as pkv
 import workloads
 from gpu_support import (assert_attention_close, assert_partials_close, on_device, run_v1,
-                         run_v2)
+                         run_v2, variant_kwargs)
 
 pytestmark = pytest.mark.gpu
 
@@ -307,6 +307,49 @@ def test_bad_device_data_sets_flags_without_faulting():
     assert int(err.item()) & pkv.PKV_ERRF_SPLITS
     # the context is still usable
     assert_attention_close(run_v1(g), _oracle_v1(inp), torch.bfloat16, "after errors")
+
+
+def _check_longest_first(order, lens):
+    o = order.cpu().tolist()
+    assert sorted(o) == list(range(len(lens))), "not a permutation"
+    ml = max(max(lens), 0)
+    buckets = [(ml - max(lens[i], 0)) * 256 // (ml + 1) for i in o]
+    assert buckets == sorted(buckets), "buckets out of order"
+
+
+def test_longest_first_order_and_decode_in_that_order():
+    """pkv_order_by_length gives a permutation whose length buckets never
+    decrease (the order within a bucket is not fixed); decoding in that order
+    gives bit-identical outputs; an entry out of range sets PKV_ERRF_ORDER."""
+    lens = [5, 1200, 0, 333, 1200, 17, 64, 900, 1, 2048]
+    inp = _inputs("bf16", 128, 16, 16, 4, lens, seed=41)
+    g = on_device(inp)
+    order = torch.empty(len(lens), dtype=torch.int32, device="cuda")
+    pkv.order_by_length(order, g["seq_lens"])
+    torch.cuda.synchronize()
+    _check_longest_first(order, lens)
+    ref = run_v1(g)
+    out = torch.empty_like(g["query"])
+    pkv.paged_attention_decode(out, g["query"], g["key_cache"], g["value_cache"],
+                               g["block_tables"], g["seq_lens"], g["scale"], seq_order=order,
+                               **variant_kwargs(g))
+    assert torch.equal(out, ref)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad = order.clone()
+    bad[3] = len(lens) + 5
+    pkv.paged_attention_decode(out, g["query"], g["key_cache"], g["value_cache"],
+                               g["block_tables"], g["seq_lens"], g["scale"], seq_order=bad,
+                               err_flag=err, **variant_kwargs(g))
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.PKV_ERRF_ORDER
+    # many sequences per thread of the ordering CTA, ties and negative lengths
+    gen = torch.Generator().manual_seed(43)
+    big = torch.randint(-3, 5000, (3000,), generator=gen, dtype=torch.int32)
+    big[:500] = 777
+    order = torch.empty(3000, dtype=torch.int32, device="cuda")
+    pkv.order_by_length(order, big.cuda())
+    torch.cuda.synchronize()
+    _check_longest_first(order, big.tolist())
 
 
 def test_copy_wait_timeout_is_reported_and_the_context_survives():
