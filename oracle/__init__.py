@@ -21,6 +21,7 @@ from .attention import (  # noqa: F401
 from .metadata import (  # noqa: F401
     cdiv,
     copy_page_indices,
+    cu_num_pages,
     decode_set_metadata,
     ext_device_core_count,
     log2_f32,

@@ -171,6 +171,25 @@ def decode_set_metadata(seq_lens, req_to_token, req_pool_indices, max_seq_pages:
     return cache, cu, page_table, swa
 
 
+def cu_num_pages(cache_seqlens: Sequence[int], page_size: int):
+    """Page-count indptr of a decode batch: ``cu[0] = 0`` and ``cu[i + 1] =
+    cu[i] + ceil(cache_seqlens[i] / page_size)`` as a running int32 sum (a
+    negative length holds no page).  It is the ``cu_num_blocks`` indptr that
+    ``copy_page_indices`` (vLLM PR 35765, ``_copy_page_indices_kernel``)
+    reads, built from the lengths the fused decode metadata produces (sglang
+    ``normal_decode_set_metadata``, ``cache_seqlens``); the pages leave its
+    construction to the caller, so this is the plain definition."""
+    if page_size <= 0:
+        raise ValueError("page_size must be positive")
+    cu = [0]
+    acc = 0
+    for n in cache_seqlens:
+        pages = cdiv(int(n), page_size) if int(n) > 0 else 0
+        acc = wrap_int32(acc + pages)
+        cu.append(acc)
+    return cu
+
+
 def swa_spec_page_table(dst, page_table_a, page_table_b, seq_len_a, seq_len_b,
                         num_draft_tokens: int):
     """sglang ``prepare_swa_spec_page_table_triton`` / ``_prepare_swa_spec_page_table_kernel``

@@ -544,6 +544,25 @@ def test_decode_set_metadata_int32_cast_wraps():
     assert cu == [0, -(2 ** 31), -(2 ** 31) + 6]
 
 
+def test_cu_num_pages_pins():
+    """The page-count indptr: a hand-worked case (page size 16, an empty and
+    a negative length hold no page), page size 1 equals the running sum of
+    the lengths, numpy's ceil-division cumsum on random lengths, and the
+    ragged workload's indptr (built there from the block rows it allocates,
+    not from this function)."""
+    assert oracle.cu_num_pages([0, 1, 16, 17, -5, 32], 16) == [0, 0, 1, 2, 4, 4, 6]
+    g = torch.Generator().manual_seed(5)
+    lens = torch.randint(0, 40000, (300,), generator=g)
+    assert oracle.cu_num_pages(lens.tolist(), 1) == [0] + np.cumsum(lens.numpy()).tolist()
+    for ps in (2, 16, 64):
+        want = [0] + np.cumsum(-(-lens.numpy() // ps)).tolist()
+        assert oracle.cu_num_pages(lens.tolist(), ps) == want
+    inp = workloads.make_workload("ragged_v2_bf16", seed=0, num_seqs=40)
+    assert oracle.cu_num_pages(inp["seq_lens_list"], 16) == inp["cu_num_blocks"].tolist()
+    # int32 running sum, as cu_seqlens_k
+    assert oracle.cu_num_pages([2 ** 31 - 1, 1], 1) == [0, 2 ** 31 - 1, -(2 ** 31)]
+
+
 # ------------------------------------------- metadata: SWA speculative table ---
 
 def _read_swa_example():
