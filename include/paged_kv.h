@@ -360,6 +360,11 @@ pkv_status_t prepare_decode_metadata(int32_t *page_indices, int64_t page_indices
  *   page_index            = req_to_token[req_pool_indices[i], c << SHIFT],  c < max_seq_pages
  *   page_table[i, c]      = page_index >> SHIFT
  *   swa_page_table[i, c]  = int32(full_to_swa_mapping[page_index] >> SHIFT)   (if given)
+ *   cu_num_pages[i]       = pages[0] + ... + pages[i-1]  (int32, i <= B; if given),
+ *                           pages[j] = ceil(cache_seqlens[j] / page_size), 0 if <= 0:
+ *                           the page-count indptr that copy_page_indices and
+ *                           prepare_decode_metadata take as cu_num_blocks, built on
+ *                           the device in the same launch
  * Bit-exact.  Every column c < max_seq_pages of every row is written, as on
  * the page.  All strides are in elements.  A pool row or column outside
  * [0, req_to_token_rows) x [0, req_to_token_cols), or a page index outside
@@ -391,6 +396,8 @@ typedef struct {
   int64_t full_to_swa_stride;
   int64_t full_to_swa_len;
   int32_t *err_flag;                  /* optional */
+  int32_t *cu_num_pages;              /* optional (NULL: not written) */
+  int64_t cu_num_pages_stride;
 } pkv_decode_metadata_args_t;
 
 pkv_status_t normal_decode_set_metadata(const pkv_decode_metadata_args_t *args,

@@ -95,6 +95,7 @@ class DecodeMetadataArgs(ctypes.Structure):
         ("full_to_swa_mapping", _c_p), ("full_to_swa_stride", _c_i64),
         ("full_to_swa_len", _c_i64),
         ("err_flag", _c_p),
+        ("cu_num_pages", _c_p), ("cu_num_pages_stride", _c_i64),
     ]
 
 
@@ -499,14 +500,15 @@ def prepare_decode_metadata(page_indices: torch.Tensor, block_table: torch.Tenso
 def decode_metadata_args(cache_seqlens, cu_seqlens_k, page_table, req_to_token, req_pool_indices,
                          seq_lens, *, seq_len_delta: int, page_size: int,
                          max_seq_pages: Optional[int] = None, swa_page_table=None,
-                         full_to_swa_mapping=None, err_flag=None) -> DecodeMetadataArgs:
+                         full_to_swa_mapping=None, err_flag=None,
+                         cu_num_pages=None) -> DecodeMetadataArgs:
     """Fill the argument struct of ``normal_decode_set_metadata`` from tensors."""
     checks = ((cache_seqlens, "cache_seqlens", torch.int32), (cu_seqlens_k, "cu_seqlens_k", torch.int32),
               (page_table, "page_table", torch.int32), (req_to_token, "req_to_token", torch.int32),
               (req_pool_indices, "req_pool_indices", torch.int64), (seq_lens, "seq_lens", torch.int64),
               (swa_page_table, "swa_page_table", torch.int32),
               (full_to_swa_mapping, "full_to_swa_mapping", torch.int64),
-              (err_flag, "err_flag", torch.int32))
+              (err_flag, "err_flag", torch.int32), (cu_num_pages, "cu_num_pages", torch.int32))
     for t, n, dt in checks:
         _cuda(t, n)
         if t is not None and t.dtype != dt:
@@ -539,20 +541,27 @@ def decode_metadata_args(cache_seqlens, cu_seqlens_k, page_table, req_to_token, 
         a.full_to_swa_stride = full_to_swa_mapping.stride(0)
         a.full_to_swa_len = full_to_swa_mapping.shape[0]
     a.err_flag = _ptr(err_flag)
+    if cu_num_pages is not None:
+        if cu_num_pages.dim() != 1 or cu_num_pages.shape[0] < B + 1:
+            raise ValueError("cu_num_pages must hold batch_size + 1 entries")
+        a.cu_num_pages, a.cu_num_pages_stride = _ptr(cu_num_pages), cu_num_pages.stride(0)
     return a
 
 
 def normal_decode_set_metadata(cache_seqlens, cu_seqlens_k, page_table, req_to_token,
                                req_pool_indices, seq_lens, *, seq_len_delta: int, page_size: int,
                                max_seq_pages: Optional[int] = None, swa_page_table=None,
-                               full_to_swa_mapping=None, err_flag=None, stream=None) -> None:
+                               full_to_swa_mapping=None, err_flag=None, cu_num_pages=None,
+                               stream=None) -> None:
     """Fused decode metadata: lengths + delta, their int32 indptr, the page
-    table gathered from ``req_to_token`` (and the sliding-window table)."""
+    table gathered from ``req_to_token`` (and the sliding-window table); with
+    ``cu_num_pages`` (int32 ``[batch_size + 1]``) also the page-count indptr
+    that the page-index copy takes as ``cu_num_blocks``."""
     a = decode_metadata_args(cache_seqlens, cu_seqlens_k, page_table, req_to_token,
                              req_pool_indices, seq_lens, seq_len_delta=seq_len_delta,
                              page_size=page_size, max_seq_pages=max_seq_pages,
                              swa_page_table=swa_page_table, full_to_swa_mapping=full_to_swa_mapping,
-                             err_flag=err_flag)
+                             err_flag=err_flag, cu_num_pages=cu_num_pages)
     _check(lib().normal_decode_set_metadata(ctypes.byref(a), _stream(stream)),
            "normal_decode_set_metadata")
 

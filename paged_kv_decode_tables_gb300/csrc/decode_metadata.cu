@@ -86,40 +86,60 @@ __global__ void __launch_bounds__(kCols) decode_metadata_kernel(const pkv_decode
   const int64_t gather_blocks = int64_t(a.batch_size) * chunks;
   if (int64_t(blockIdx.x) == gather_blocks) {
     // lengths and their exclusive scan (int32 arithmetic, wrapping like a cast)
-    __shared__ unsigned warp_sum[kCols / 32];
-    __shared__ unsigned carry_s;
+    // With cu_num_pages, the page counts ceil(len / page_size) (0 for a
+    // length <= 0) are scanned alongside, in the same int32 arithmetic.
+    __shared__ unsigned warp_sum[2][kCols / 32];
     const int lane = tid & 31, warp = tid >> 5;
-    unsigned carry = 0;
+    const bool pages_out = a.cu_num_pages != nullptr;
+    unsigned carry = 0, carry_p = 0;
     for (int base = 0; base < a.batch_size; base += kCols) {
       const int i = base + tid;
-      unsigned v = 0;
+      unsigned v = 0, np = 0;
       if (i < a.batch_size) {
         v = unsigned(a.seq_lens[int64_t(i) * a.seq_lens_stride] + a.seq_len_delta);
         a.cache_seqlens[int64_t(i) * a.cache_seqlens_stride] = int32_t(v);
+        np = int32_t(v) > 0 ? ((v - 1u) >> shift) + 1u : 0u;
       }
-      unsigned incl = v;
+      unsigned incl = v, incl_p = np;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const unsigned t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
+        const unsigned tp = __shfl_up_sync(0xffffffffu, incl_p, o);
+        if (lane >= o) {
+          incl += t;
+          incl_p += tp;
+        }
       }
-      if (lane == 31) warp_sum[warp] = incl;
+      if (lane == 31) {
+        warp_sum[0][warp] = incl;
+        warp_sum[1][warp] = incl_p;
+      }
       __syncthreads();
-      unsigned before = 0, total = 0;
+      unsigned before = 0, total = 0, before_p = 0, total_p = 0;
 #pragma unroll
       for (int w = 0; w < kCols / 32; ++w) {
-        const unsigned ws = warp_sum[w];
-        if (w < warp) before += ws;
+        const unsigned ws = warp_sum[0][w], wp = warp_sum[1][w];
+        if (w < warp) {
+          before += ws;
+          before_p += wp;
+        }
         total += ws;
+        total_p += wp;
       }
-      if (i < a.batch_size)
+      if (i < a.batch_size) {
         a.cu_seqlens_k[int64_t(i) * a.cu_seqlens_k_stride] = int32_t(carry + before + incl - v);
+        if (pages_out)
+          a.cu_num_pages[int64_t(i) * a.cu_num_pages_stride] =
+              int32_t(carry_p + before_p + incl_p - np);
+      }
       carry += total;
+      carry_p += total_p;
       __syncthreads();
     }
     if (tid == 0) {
-      carry_s = carry;
-      a.cu_seqlens_k[int64_t(a.batch_size) * a.cu_seqlens_k_stride] = int32_t(carry_s);
+      a.cu_seqlens_k[int64_t(a.batch_size) * a.cu_seqlens_k_stride] = int32_t(carry);
+      if (pages_out)
+        a.cu_num_pages[int64_t(a.batch_size) * a.cu_num_pages_stride] = int32_t(carry_p);
     }
     return;
   }

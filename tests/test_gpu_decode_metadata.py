@@ -147,3 +147,49 @@ def test_decode_metadata_row_copy_short_and_bad_rows():
     assert got[1, :130].tolist() == [0] * 130
     assert got[2, :100].tolist() == list(range(0, 100)) and got[2, 100:130].tolist() == [0] * 30
     assert got[:, 130:].tolist() == [[-1, -1]] * 3
+
+
+@pytest.mark.parametrize("page_size", [1, 16, 64])
+@pytest.mark.parametrize("strided", [False, True])
+def test_decode_metadata_page_count_indptr(page_size, strided):
+    """The optional cu_num_pages output equals the oracle's page-count indptr
+    bit for bit: 700 rows (three rounds of the scan), a length that turns
+    negative with the delta, strided output; the other outputs unchanged."""
+    B, msp = 700, 4
+    g = torch.Generator().manual_seed(61 + page_size)
+    pool_rows, cols = B + 3, msp * page_size
+    rt = torch.randint(0, 1 << 22, (pool_rows, cols), generator=g, dtype=torch.int32)
+    pool = torch.randperm(pool_rows, generator=g)[:B].to(torch.int64)
+    lens = torch.randint(0, 70000, (B,), generator=g, dtype=torch.int64)
+    lens[3], lens[4] = -5, 0
+    dev = "cuda"
+    cache = torch.empty(B, dtype=torch.int32, device=dev)
+    cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    pt = torch.empty(B, msp, dtype=torch.int32, device=dev)
+    store = torch.full((2 * (B + 1),), -9, dtype=torch.int32, device=dev)
+    cup = store[::2] if strided else store[:B + 1]
+    pkv.normal_decode_set_metadata(cache, cu, pt, rt.to(dev), pool.to(dev), lens.to(dev),
+                                   seq_len_delta=1, page_size=page_size, max_seq_pages=msp,
+                                   cu_num_pages=cup)
+    want_cache, want_cu, want_pt, _ = oracle.decode_set_metadata(lens.tolist(), rt, pool.tolist(),
+                                                                 msp, 1, page_size)
+    assert cup.tolist() == oracle.cu_num_pages(want_cache, page_size)
+    assert cache.tolist() == want_cache and cu.tolist() == want_cu and pt.tolist() == want_pt
+    if strided:
+        assert bool((store[1::2] == -9).all())
+
+
+def test_decode_metadata_page_count_indptr_int32_wrap():
+    dev = "cuda"
+    lens = torch.tensor([2 ** 31 - 1, 5], dtype=torch.int64, device=dev)
+    cache = torch.empty(2, dtype=torch.int32, device=dev)
+    cu = torch.empty(3, dtype=torch.int32, device=dev)
+    cup = torch.empty(3, dtype=torch.int32, device=dev)
+    pt = torch.empty(2, 1, dtype=torch.int32, device=dev)
+    rt = torch.zeros(1, 1, dtype=torch.int32, device=dev)
+    pool = torch.zeros(2, dtype=torch.int64, device=dev)
+    pkv.normal_decode_set_metadata(cache, cu, pt, rt, pool, lens, seq_len_delta=1, page_size=1,
+                                   max_seq_pages=0, cu_num_pages=cup)
+    want_cache = [-(2 ** 31), 6]
+    assert cache.tolist() == want_cache
+    assert cup.tolist() == oracle.cu_num_pages(want_cache, 1) == [0, 0, 6]
