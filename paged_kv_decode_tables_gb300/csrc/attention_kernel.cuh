@@ -137,7 +137,8 @@ struct AttnCfg {
   static constexpr int kBarOffset = WARPS * (kWarpBytes + kPBytes);
   static constexpr int kSmemBytes = kBarOffset + WARPS * kStages * 8;
   static constexpr int kThreads = WARPS * 32;
-  static_assert(kEpiFloats * 4 <= kWarpBytes, "epilogue does not fit the warp's stages");
+  static_assert((kEpiFloats + (WARPS + 1) * kMaxGroup) * 4 <= kWarpBytes,
+                "epilogue does not fit the warp's stages");
   static_assert(D % 32 == 0 && BS % 8 == 0, "unsupported shape");
   static_assert(kHalfStage % 16 == 0 && kPageBytes % 16 == 0, "bulk copies need 16 B");
   static_assert(kPBytes % 16 == 0 && (kPRow * 4) % 16 == 0, "16-byte probability rows");
@@ -1189,6 +1190,41 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
   }
 
   // ---------------------------------------------- combine warps, write out --
+  // Per head, once: the warps' weights 2^(m_w - M), the total L and the
+  // output factor out_scale / L (and the split-KV statistics); then every
+  // element is a weighted sum of the warps' rows and one multiply.
+  // They sit in warp 0's ring after its epilogue rows (every copy has landed).
+  float(*head_w)[kMaxGroup] =
+      reinterpret_cast<float(*)[kMaxGroup]>(smem + Cfg::kEpiFloats * 4);
+  float *head_fac = reinterpret_cast<float *>(smem + Cfg::kEpiFloats * 4) + WARPS * kMaxGroup;
+  if constexpr (WARPS > 1) {
+    __syncthreads();
+  } else {
+    __syncwarp();
+  }
+  if (threadIdx.x < g) {
+    const int h = threadIdx.x;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float *ew = reinterpret_cast<const float *>(smem + w * Cfg::kWarpBytes);
+      M = fmaxf(M, ew[kMaxGroup * D + h]);
+    }
+    float Ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float *ew = reinterpret_cast<const float *>(smem + w * Cfg::kWarpBytes);
+      const float f = ex2(ew[kMaxGroup * D + h] - M);
+      head_w[w][h] = f;
+      Ls = fmaf(f, ew[kMaxGroup * D + kMaxGroup + h], Ls);
+    }
+    head_fac[h] = __fdiv_rn(p.out_scale, Ls);
+    if (p.mode != kModeV1) {
+      const int64_t row = (int64_t(seq) * p.num_heads + h0 + h) * p.max_parts + part;
+      p.es[row] = Ls;
+      p.ml[row] = M * kLn2;
+    }
+  }
   if constexpr (WARPS > 1) {
     __syncthreads();
   } else {
@@ -1196,31 +1232,19 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
   }
   for (int idx = threadIdx.x; idx < g * D; idx += WARPS * 32) {
     const int h = idx / D, d = idx % D;
-    float M = -INFINITY;
+    float O = 0.f;
 #pragma unroll
     for (int w = 0; w < WARPS; ++w) {
       const float *ew = reinterpret_cast<const float *>(smem + w * Cfg::kWarpBytes);
-      M = fmaxf(M, ew[kMaxGroup * D + h]);
+      O = fmaf(head_w[w][h], ew[h * D + d], O);
     }
-    float Ls = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) {
-      const float *ew = reinterpret_cast<const float *>(smem + w * Cfg::kWarpBytes);
-      const float f = ex2(ew[kMaxGroup * D + h] - M);
-      Ls = fmaf(f, ew[kMaxGroup * D + kMaxGroup + h], Ls);
-      O = fmaf(f, ew[h * D + d], O);
-    }
-    const float r = __fdiv_rn(O * p.out_scale, Ls);
+    const float r = O * head_fac[h];
     if (p.mode == kModeV1) {
       T *out = static_cast<T *>(p.out);
       out[int64_t(seq) * p.o_s0 + int64_t(h0 + h) * p.o_s1 + int64_t(d) * p.o_s2] = from_f32<T>(r);
     } else {
       const int64_t row = (int64_t(seq) * p.num_heads + h0 + h) * p.max_parts + part;
       p.tmp[row * D + d] = r;
-      if (d == 0) {
-        p.es[row] = Ls;
-        p.ml[row] = M * kLn2;
-      }
     }
   }
 }
