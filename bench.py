@@ -197,7 +197,7 @@ class DecodeStep:
     straight through the C ABI with argument structs prepared once."""
 
     def __init__(self, name: str, seed: int, device, num_seqs=None, fused_metadata=True,
-                 lpt=False):
+                 lpt=False, seq_len=None):
         import ctypes
 
         import paged_kv_decode_tables_gb300 as pkv
@@ -206,10 +206,14 @@ class DecodeStep:
         self.lib = pkv.lib()
         self.name = name
         over = {} if num_seqs is None else {"num_seqs": num_seqs}
+        if seq_len is not None:
+            n = num_seqs if num_seqs is not None else workloads.WORKLOADS[name].num_seqs
+            over.update(seq_len_recipe="fixed", seq_lens=[int(seq_len)] * n)
         inp = workloads.make_workload(name, seed=seed, device=device, **over)
         self.inp = inp
         spec = inp["spec"]
         self.spec = spec
+        self._input_arena(inp)
         q, kc, vc = inp["query"], inp["key_cache"], inp["value_cache"]
         B, H, D = q.shape
         Hk, bs = kc.shape[1], kc.shape[3]
@@ -269,6 +273,39 @@ class DecodeStep:
                                (self.out_bytes if self.mode == "v1" else 0) +
                                (4 * B + 4 * (B + 1) if self.mode == "v2_splits" else 0) +
                                (4 * H if spec.alibi else 0))
+
+    def _input_arena(self, inp):
+        """Place the per-step inputs (query, lengths, indptr, the table or a
+        packed copy of its strided view) in one device buffer, so that an
+        end-to-end step brings them in with a single host-to-device copy (a
+        pinned copy costs about 11 us before its first byte on this link).
+        The step's tensors become views of that buffer; a strided table view
+        is filled from its packed copy by a device copy."""
+        parts = [("query", inp["query"]), ("seq_lens", inp["seq_lens"])]
+        if "cu_num_blocks" in inp:
+            parts.append(("cu_num_blocks", inp["cu_num_blocks"]))
+        bt = inp["block_tables"]
+        parts.append(("table", bt))
+        layout, off = {}, 0
+        for name, t in parts:
+            off = -(-off // 256) * 256
+            n = t.numel() * t.element_size()
+            layout[name] = (off, n, t.dtype, tuple(t.shape))
+            off += n
+        arena = torch.empty(off, dtype=torch.uint8, device=bt.device)
+        views = {name: arena[o:o + n].view(dt).view(shape)
+                 for name, (o, n, dt, shape) in layout.items()}
+        for name, t in parts:
+            views[name].copy_(t)
+        self.arena = arena
+        for name in ("query", "seq_lens", "cu_num_blocks"):
+            if name in views:
+                inp[name] = views[name]
+        if bt.is_contiguous():
+            inp["block_tables"] = views["table"]
+            self._table_stage = None
+        else:
+            self._table_stage = views["table"]
 
     def _check(self, st, what):
         if st != 0:
@@ -352,35 +389,20 @@ class DecodeStep:
         return workload_config(self.inp, world)
 
     def host_inputs(self):
-        """Pinned host copies of the per-step inputs (query, lengths, the live
-        block-table view packed row by row, indptr) and a pinned host buffer for
-        the result.  Only the table's view is sent, not its backing storage (a
+        """A pinned host copy of the input buffer (query, lengths, indptr, the
+        table's live view packed row by row) and a pinned host buffer for the
+        result.  Only the table's view is sent, not its backing storage (a
         stride-2 view covers half of it)."""
-        inp = self.inp
-        hin = {"query": inp["query"].cpu().pin_memory(),
-               "seq_lens": inp["seq_lens"].cpu().pin_memory(),
-               "table": inp["block_tables"].cpu().contiguous().pin_memory()}
-        if self.mode == "v2_splits":
-            hin["cu"] = self.cu.cpu().pin_memory()
-        self._table_stage = (None if inp["block_tables"].is_contiguous() else
-                             torch.empty(hin["table"].shape, dtype=torch.int32,
-                                         device=inp["block_tables"].device))
+        hin = {"arena": self.arena.cpu().pin_memory()}
         hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         return hin, hout
 
     def e2e_enqueue(self, hin, hout):
-        """H2D of the step's inputs, the step, D2H of its output (enqueued only).
-        A strided table view is filled from a packed device copy."""
-        inp = self.inp
-        inp["query"].copy_(hin["query"], non_blocking=True)
-        inp["seq_lens"].copy_(hin["seq_lens"], non_blocking=True)
-        if self._table_stage is None:
-            inp["block_tables"].copy_(hin["table"], non_blocking=True)
-        else:
-            self._table_stage.copy_(hin["table"], non_blocking=True)
-            inp["block_tables"].copy_(self._table_stage)
-        if "cu" in hin:
-            self.cu.copy_(hin["cu"], non_blocking=True)
+        """H2D of the step's inputs (one copy), the step, D2H of its output
+        (enqueued only).  A strided table view is filled from its packed copy."""
+        self.arena.copy_(hin["arena"], non_blocking=True)
+        if self._table_stage is not None:
+            self.inp["block_tables"].copy_(self._table_stage)
         self.run()
         hout.copy_(self.out, non_blocking=True)
 
@@ -784,7 +806,8 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     step = DecodeStep(args.workload, seed=rank, device="cuda", num_seqs=args.num_seqs,
-                      fused_metadata=args.metadata == "fused", lpt=args.lpt)
+                      fused_metadata=args.metadata == "fused", lpt=args.lpt,
+                      seq_len=args.seq_len)
     if args.warps:
         step.pkv.set_attention_warps(args.warps)
     if args.fp8_kernel == "tensor-memory":
@@ -831,7 +854,9 @@ def run_ours(args):
     ms_step = elapsed_ms / K
     value = aggregate_gbs(step.kv_bytes, world, ms_step * 1e-3)
     peak, peak_kind = load_peak()
-    roofline = roofline_record(step, attn_ms, peak, peak_kind, args.workload)
+    # the committed DRAM record is for the full batch, not a cut or resized one
+    full = args.num_seqs is None and args.seq_len is None
+    roofline = roofline_record(step, attn_ms, peak, peak_kind, args.workload if full else None)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(step.inp, spec, budget_s=args.cpu_budget)
@@ -865,16 +890,16 @@ def run_ours(args):
         "e2e": {"value": round(aggregate_gbs(step.kv_bytes, world, e2e_s / Ke), 2), "unit": UNIT,
                 "us_per_step": round(e2e_s / Ke * 1e6, 2), "steps": Ke,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": ("K/V cache resident on the device; per step: H2D of the inputs (the "
-                         "table as its packed live view) from pinned host memory, the step, D2H "
-                         "of the output, host waits"
+                "note": ("K/V cache resident on the device; per step: one H2D copy of the "
+                         "inputs (query, lengths, indptr, the table as its packed live view) "
+                         "from one pinned host buffer, the step, D2H of the output, host waits"
                          + ("; replayed as one CUDA graph" if e2e_graph is not None else "")),
                 "graph": e2e_graph is not None},
         "gpu_launches": K * step.launches_per_step,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
-    if world == 1 and not args.no_companions and args.num_seqs is None:
+    if world == 1 and not args.no_companions and args.num_seqs is None and args.seq_len is None:
         # the other configurations, one after another with the same steps and
         # warm-up; the headline's buffers are released first
         del step, hin, hout, e2e_graph
@@ -1080,6 +1105,8 @@ def main(argv=None):
                     + sorted(workloads.SWA_SPEC_WORKLOADS))
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="smaller batch of the same workload (profiling captures only)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="every sequence this many tokens (launch-size sweeps only)")
     ap.add_argument("--warps", type=int, default=0, choices=[0, 1, 2, 4],
                     help="force warps per attention CTA (0: library default)")
     ap.add_argument("--fp8-kernel", choices=["mma", "tensor-memory"], default="mma",

@@ -93,3 +93,21 @@ def test_full_size_workload(name):
                                                  num_kv_splits=[splits[s] for s in seqs], **kw)
         assert_partials_close(step.tmp[sel], step.es[sel], step.ml[sel], rtmp, res, rml,
                               f"{name} sampled partials")
+
+
+@pytest.mark.parametrize("name", ["ragged_v2_bf16", "gqa_v1_bf16", "long_v2_fp8"])
+def test_end_to_end_step_equals_device_step(name):
+    """The end-to-end step (one host-to-device copy of the input buffer, the
+    step, the output copied back) reproduces the device-resident step bit for
+    bit, after every device-side input has been overwritten."""
+    step = _run_step(name)
+    want = step.out.cpu()
+    hin, hout = step.host_inputs()
+    step.arena.fill_(0xFF)
+    step.inp["block_tables"].fill_(-1)
+    step.out.zero_()
+    step.e2e_enqueue(hin, hout)
+    torch.cuda.synchronize()
+    assert torch.equal(hout, want)
+    h2d, d2h = step.e2e_bytes(hin, hout)
+    assert h2d == step.arena.numel() and d2h == want.numel() * want.element_size()
