@@ -197,7 +197,7 @@ class DecodeStep:
     straight through the C ABI with argument structs prepared once."""
 
     def __init__(self, name: str, seed: int, device, num_seqs=None, fused_metadata=True,
-                 lpt=False, seq_len=None):
+                 lpt=False, seq_len=None, partition_size=None):
         import ctypes
 
         import paged_kv_decode_tables_gb300 as pkv
@@ -209,6 +209,8 @@ class DecodeStep:
         if seq_len is not None:
             n = num_seqs if num_seqs is not None else workloads.WORKLOADS[name].num_seqs
             over.update(seq_len_recipe="fixed", seq_lens=[int(seq_len)] * n)
+        if partition_size is not None:
+            over["partition_size"] = int(partition_size)
         inp = workloads.make_workload(name, seed=seed, device=device, **over)
         self.inp = inp
         spec = inp["spec"]
@@ -807,7 +809,7 @@ def run_ours(args):
         dist.barrier()
     step = DecodeStep(args.workload, seed=rank, device="cuda", num_seqs=args.num_seqs,
                       fused_metadata=args.metadata == "fused", lpt=args.lpt,
-                      seq_len=args.seq_len)
+                      seq_len=args.seq_len, partition_size=args.partition_size)
     if args.warps:
         step.pkv.set_attention_warps(args.warps)
     if args.fp8_kernel == "tensor-memory":
@@ -855,7 +857,7 @@ def run_ours(args):
     value = aggregate_gbs(step.kv_bytes, world, ms_step * 1e-3)
     peak, peak_kind = load_peak()
     # the committed DRAM record is for the full batch, not a cut or resized one
-    full = args.num_seqs is None and args.seq_len is None
+    full = (args.num_seqs, args.seq_len, args.partition_size) == (None, None, None)
     roofline = roofline_record(step, attn_ms, peak, peak_kind, args.workload if full else None)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -899,7 +901,8 @@ def run_ours(args):
         "clocks": clk,
         "cpu_baseline": cpu,
     }
-    if world == 1 and not args.no_companions and args.num_seqs is None and args.seq_len is None:
+    resized = (args.num_seqs, args.seq_len, args.partition_size) != (None, None, None)
+    if world == 1 and not args.no_companions and not resized:
         # the other configurations, one after another with the same steps and
         # warm-up; the headline's buffers are released first
         del step, hin, hout, e2e_graph
@@ -1107,6 +1110,8 @@ def main(argv=None):
                     help="smaller batch of the same workload (profiling captures only)")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="every sequence this many tokens (launch-size sweeps only)")
+    ap.add_argument("--partition-size", type=int, default=None,
+                    help="tokens per partition of a fixed-partition workload (sweeps only)")
     ap.add_argument("--warps", type=int, default=0, choices=[0, 1, 2, 4],
                     help="force warps per attention CTA (0: library default)")
     ap.add_argument("--fp8-kernel", choices=["mma", "tensor-memory"], default="mma",
