@@ -80,7 +80,7 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-ATTENTION_SOURCES = ("attention_kernel.cuh", "pkv_ptx.cuh")
+ATTENTION_SOURCES = ("attention_kernel.cuh", "attention_unit.inc", "pkv_ptx.cuh")
 METADATA_SOURCES = ("decode_metadata.cu", "pkv_ptx.cuh", "pkv_launch.cuh")
 
 

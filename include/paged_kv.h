@@ -193,6 +193,21 @@ pkv_status_t pkv_set_attention_warps(int32_t warps);
 pkv_status_t pkv_set_fp8_kernel(int32_t which);
 
 /*
+ * Split-KV partition pass (paged_attention_v2_partition with num_kv_splits)
+ * over an fp8 cache on two warps per CTA (block size below 32, the mma.sync
+ * kernel): 1 (default) launches ceil(max_num_partitions / 2) partition slots
+ * per (kv head x head sub-group, sequence), and the CTA of slot x also runs
+ * partition x + that count of its sequence when there is one; 0 launches one
+ * CTA per partition slot.  Process-wide; a tuning and test override.  Both
+ * give bit-identical outputs.  A sequence fills num_kv_splits[seq] of the
+ * slots (on the ragged serving batch 1206 of 8192); an empty slot's CTA still
+ * holds a residency slot while it reads the sequence's length and split
+ * count, about 0.6 ns of launch time each for the latency-bound fp8 kernel.
+ * Returns PKV_ERR_INVALID_ARG for any value but 0 and 1.
+ */
+pkv_status_t pkv_set_split_fold(int32_t on);
+
+/*
  * Limit, in nanoseconds, of every wait of the attention kernels for a stage's
  * copies into shared memory (default 2 s; 0 restores it; at most 60 s).  A
  * wait that runs out sets PKV_ERRF_TIMEOUT, waits (again bounded) for the

@@ -140,6 +140,8 @@ def lib() -> ctypes.CDLL:
     L.pkv_set_attention_warps.argtypes = [_c_i32]
     L.pkv_set_fp8_kernel.restype = ctypes.c_int
     L.pkv_set_fp8_kernel.argtypes = [_c_i32]
+    L.pkv_set_split_fold.restype = ctypes.c_int
+    L.pkv_set_split_fold.argtypes = [_c_i32]
     L.pkv_set_wait_limit_ns.restype = ctypes.c_int
     L.pkv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.pkv_test_set_unarrived_bytes.restype = ctypes.c_int
@@ -226,6 +228,13 @@ def set_fp8_kernel(which: int) -> None:
     """Kernel for fp8 caches (head size 128, block size 16): 0 the mma.sync
     kernel (default), 1 the tensor-memory kernel (see ``pkv_set_fp8_kernel``)."""
     _check(lib().pkv_set_fp8_kernel(int(which)), "pkv_set_fp8_kernel")
+
+
+def set_split_fold(on: int) -> None:
+    """Split-KV over an fp8 cache on two-warp CTAs: 1 (default) half the
+    partition slots, each CTA taking a second partition of its sequence; 0 one
+    CTA per slot (see ``pkv_set_split_fold``)."""
+    _check(lib().pkv_set_split_fold(int(on)), "pkv_set_split_fold")
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -22,6 +22,7 @@ std::atomic<int> g_forced_warps{0};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<unsigned> g_extra_expect_tx{0};
 std::atomic<int> g_fp8_kernel{0};
+std::atomic<int> g_split_fold{1};
 
 int sm_count() {
   int dev = 0;
@@ -158,6 +159,7 @@ AttnParams make_params(const pkv_decode_args_t *a) {
   p.out_scale = fp8 ? a->v_scale : 1.0f;
   p.alibi = a->alibi_slopes;
   p.order = nullptr;  // set by paged_attention_decode only
+  p.fold = 0;
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   // The test hook is one-shot: the launch that reads it clears it, so a hook
   // left set can delay at most one launch, never every later one.
@@ -238,6 +240,12 @@ pkv_status_t pkv_set_attention_warps(int32_t warps) {
   return PKV_OK;
 }
 
+pkv_status_t pkv_set_split_fold(int32_t on) {
+  if (on != 0 && on != 1) return PKV_ERR_INVALID_ARG;
+  g_split_fold.store(on, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
 pkv_status_t pkv_set_fp8_kernel(int32_t which) {
   if (which != 0 && which != 1) return PKV_ERR_INVALID_ARG;
   g_fp8_kernel.store(which, std::memory_order_relaxed);
@@ -303,6 +311,17 @@ pkv_status_t paged_attention_v2_partition(float *tmp_out, float *exp_sums, float
   const int64_t units = int64_t(max_num_partitions) * grid.y * args->num_seqs;
   const int w = pick_warps(args, units, num_kv_splits ? Pass::kSplits : Pass::kFixed,
                            partition_size);
+  // Split-KV over an fp8 cache on two warps per CTA: a sequence fills
+  // num_kv_splits[seq] of the max_num_partitions slots, and an empty slot's
+  // CTA costs the latency-bound fp8 kernel about 0.6 ns of launch time.  Half
+  // the slots, each CTA taking partitions x and x + slots of its sequence,
+  // leave fewer empty CTAs (the instance runs its second partition without a
+  // further launch).
+  if (num_kv_splits && is_fp8_cache(args->kv_cache_dtype) && w == 2 && max_num_partitions >= 2 &&
+      g_split_fold.load(std::memory_order_relaxed) != 0) {
+    p.fold = 1;
+    grid.x = unsigned((max_num_partitions + 1) / 2);
+  }
   return pkv::launch_attention(args->dtype, pkv_kv_cache_dtype_t(args->kv_cache_dtype), p,
                                args->head_size, args->block_size, w, grid,
                                reinterpret_cast<cudaStream_t>(stream));

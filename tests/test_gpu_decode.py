@@ -10,7 +10,7 @@ import oracle
 import paged_kv_decode_tables_gb300 as pkv
 import workloads
 from gpu_support import (assert_attention_close, assert_partials_close, on_device, run_v1,
-                         run_v2, variant_kwargs)
+                         run_v2, variant_kwargs, oracle_kwargs)
 
 pytestmark = pytest.mark.gpu
 
@@ -433,3 +433,48 @@ def test_groups_larger_than_eight(dtype, D, bs, H, Hk):
     splits = torch.tensor([1, 2, 3, 1], dtype=torch.int32, device="cuda")
     _, _, _, out = run_v2(g, 4, splits=splits)
     assert_attention_close(out, ref, DT[dtype], f"v2 splits {H}/{Hk}")
+
+
+def _same(a, b):
+    return bool(((a == b) | (torch.isnan(a) & torch.isnan(b))).all())
+
+
+@pytest.mark.parametrize("dtype,kv,D,bs,H,Hk,maxP", [
+    ("f16", "fp8_e4m3", 128, 16, 32, 8, 16), ("bf16", "fp8_e4m3", 128, 16, 64, 8, 16),
+    ("bf16", "fp8_e5m2", 64, 8, 16, 4, 9), ("f16", "fp8_e4m3", 256, 16, 72, 4, 5),
+    ("bf16", "fp8_e4m3", 128, 16, 8, 8, 2)])
+def test_split_fold_is_bitwise_identical(dtype, kv, D, bs, H, Hk, maxP):
+    """Split-KV over an fp8 cache with half the partition slots (a CTA runs
+    partitions x and x + slots of its sequence) gives bit-identical partials,
+    statistics and outputs to one CTA per slot, for even and odd
+    max_num_partitions, head groups of 1 to 18 and zero-length sequences;
+    every (sequence, partition) row of the statistics is written."""
+    rng = torch.Generator().manual_seed(43)
+    lens = [int(x) for x in torch.randint(1, 3000, (40,), generator=rng)]
+    lens[:6] = [0, 1, 16, 17, 4096, 0]
+    inp = _inputs(dtype, D, bs, H, Hk, lens, seed=43, kv_cache_dtype=kv, k_scale=0.5,
+                  v_scale=2.0)
+    g = on_device(inp)
+    splits = torch.empty(len(lens), dtype=torch.int32, device="cuda")
+    pkv.compute_num_kv_splits(splits, g["seq_lens"], num_group=1, num_head=H, num_kv_head=Hk,
+                              max_kv_splits=maxP, device_core_count=148)
+    s = splits.cpu()
+    s[2] = maxP  # as many splits as slots on 17 tokens: some of them empty
+    s[4] = maxP - 1 if maxP > 1 else 1
+    splits = s.to("cuda")
+    try:
+        pkv.set_split_fold(0)
+        full = run_v2(g, maxP, splits=splits)
+        pkv.set_split_fold(1)
+        folded = run_v2(g, maxP, splits=splits)
+    finally:
+        pkv.set_split_fold(1)
+    for a, b, what in zip(full, folded, ("tmp_out", "exp_sums", "max_logits", "output")):
+        assert _same(a, b), f"{what} differs between one and two partitions per CTA"
+    tmp, es, ml, _ = folded
+    assert not bool(torch.isnan(es).any()) and not bool(torch.isnan(ml).any())
+    n = 8  # the oracle on the first sequences (zero lengths and full split counts among them)
+    rtmp, res, rml = oracle.v2_partition(inp["query"][:n], inp["key_cache"], inp["value_cache"],
+                                         inp["block_tables"][:n], lens[:n], inp["scale"], maxP,
+                                         num_kv_splits=s.tolist()[:n], **oracle_kwargs(inp))
+    assert_partials_close(tmp[:n], es[:n], ml[:n], rtmp, res, rml, "two partitions per CTA")
