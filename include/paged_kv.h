@@ -195,17 +195,22 @@ pkv_status_t pkv_set_fp8_kernel(int32_t which);
 /*
  * Split-KV partition pass (paged_attention_v2_partition with num_kv_splits)
  * over an fp8 cache on two warps per CTA (block size below 32, the mma.sync
- * kernel): 1 (default) launches ceil(max_num_partitions / 2) partition slots
- * per (kv head x head sub-group, sequence), and the CTA of slot x also runs
- * partition x + that count of its sequence when there is one; 0 launches one
- * CTA per partition slot.  Process-wide; a tuning and test override.  Both
- * give bit-identical outputs.  A sequence fills num_kv_splits[seq] of the
- * slots (on the ragged serving batch 1206 of 8192); an empty slot's CTA still
- * holds a residency slot while it reads the sequence's length and split
- * count, about 0.6 ns of launch time each for the latency-bound fp8 kernel.
- * Returns PKV_ERR_INVALID_ARG for any value but 0 and 1.
+ * kernel), process-wide; a tuning and test override:
+ *   1 (default): when the (sequence, kv head x head sub-group) pairs number
+ *      at least twice the GPU's resident CTAs, launch
+ *      ceil(max_num_partitions / 2) partition slots per pair, the CTA of
+ *      slot x also running partition x + that count of its sequence when
+ *      there is one; otherwise one CTA per partition slot;
+ *   2: always the halved grid;  0: always one CTA per partition slot.
+ * Every setting gives bit-identical outputs.  A sequence fills
+ * num_kv_splits[seq] of the slots (on the ragged serving batch 1206 of
+ * 8192); an empty slot's CTA still holds a residency slot while it reads the
+ * sequence's length and split count, about 0.6 ns of launch time each for the
+ * latency-bound fp8 kernel.  A sequence with more splits than slots runs two
+ * partitions back to back, which costs more than it saves on small batches.
+ * Returns PKV_ERR_INVALID_ARG for any value outside 0..2.
  */
-pkv_status_t pkv_set_split_fold(int32_t on);
+pkv_status_t pkv_set_split_fold(int32_t mode);
 
 /*
  * Limit, in nanoseconds, of every wait of the attention kernels for a stage's

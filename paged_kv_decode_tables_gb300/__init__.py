@@ -230,11 +230,11 @@ def set_fp8_kernel(which: int) -> None:
     _check(lib().pkv_set_fp8_kernel(int(which)), "pkv_set_fp8_kernel")
 
 
-def set_split_fold(on: int) -> None:
+def set_split_fold(mode: int) -> None:
     """Split-KV over an fp8 cache on two-warp CTAs: 1 (default) half the
-    partition slots, each CTA taking a second partition of its sequence; 0 one
-    CTA per slot (see ``pkv_set_split_fold``)."""
-    _check(lib().pkv_set_split_fold(int(on)), "pkv_set_split_fold")
+    partition slots with two partitions per CTA on batches that fill the GPU
+    twice, 2 always, 0 never (see ``pkv_set_split_fold``)."""
+    _check(lib().pkv_set_split_fold(int(mode)), "pkv_set_split_fold")
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -241,9 +241,10 @@ def test_reduce_and_metadata_reject_bad_arguments(lib):
     assert lib.pkv_set_fp8_kernel(2) == 1
     assert lib.pkv_set_fp8_kernel(-1) == 1
     assert lib.pkv_set_fp8_kernel(0) == 0
-    assert lib.pkv_set_split_fold(2) == 1
+    assert lib.pkv_set_split_fold(3) == 1
     assert lib.pkv_set_split_fold(-1) == 1
     assert lib.pkv_set_split_fold(0) == 0
+    assert lib.pkv_set_split_fold(2) == 0
     assert lib.pkv_set_split_fold(1) == 0
     assert lib.pkv_order_by_length(p, p, -1, None) == 1
     assert lib.pkv_order_by_length(None, p, 4, None) == 1
