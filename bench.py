@@ -173,6 +173,19 @@ def flushes_l2(inp) -> bool:
     return kv_bytes_of(inp) < 4 * L2_BYTES
 
 
+def workload_overrides(name: str, num_seqs=None, seq_len=None, partition_size=None) -> dict:
+    """Spec fields that a cut or resized batch replaces (profiling and sweeps
+    only): fewer sequences, every sequence `seq_len` tokens, another fixed
+    partition size.  Both arms apply the same ones."""
+    over = {} if num_seqs is None else {"num_seqs": num_seqs}
+    if seq_len is not None:
+        n = num_seqs if num_seqs is not None else workloads.WORKLOADS[name].num_seqs
+        over.update(seq_len_recipe="fixed", seq_lens=[int(seq_len)] * n)
+    if partition_size is not None:
+        over["partition_size"] = int(partition_size)
+    return over
+
+
 def workload_config(inp, world: int = 1) -> dict:
     """The workload's identifying configuration: the same dict in both arms."""
     spec = inp["spec"]
@@ -205,12 +218,7 @@ class DecodeStep:
         self.pkv = pkv
         self.lib = pkv.lib()
         self.name = name
-        over = {} if num_seqs is None else {"num_seqs": num_seqs}
-        if seq_len is not None:
-            n = num_seqs if num_seqs is not None else workloads.WORKLOADS[name].num_seqs
-            over.update(seq_len_recipe="fixed", seq_lens=[int(seq_len)] * n)
-        if partition_size is not None:
-            over["partition_size"] = int(partition_size)
+        over = workload_overrides(name, num_seqs, seq_len, partition_size)
         inp = workloads.make_workload(name, seed=seed, device=device, **over)
         self.inp = inp
         spec = inp["spec"]
@@ -554,9 +562,10 @@ def run_reference(args):
     rank, world, _ = env_rank()
     if rank != 0:
         return 0
-    spec = workloads.WORKLOADS[args.workload]
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = workloads.make_workload(args.workload, seed=0, device=device)
+    over = workload_overrides(args.workload, args.num_seqs, args.seq_len, args.partition_size)
+    inp = workloads.make_workload(args.workload, seed=0, device=device, **over)
+    spec = inp["spec"]
     cores = cpu_threads()
     # the whole --steps K --warmup W run stays within the budget: each step
     # processes sequences (at least one) for its share of it

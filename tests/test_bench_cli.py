@@ -87,3 +87,25 @@ def test_step_statistics():
     assert st["p10"] <= st["median"] <= st["p90"]
     assert st["median"] == round(bench.percentile(sorted(ms), 0.5) * 1e3, 2)
     assert bench.percentile([1.0], 0.9) == 1.0
+
+
+def test_reference_arm_applies_the_batch_overrides():
+    """A cut or resized batch (--num-seqs, --seq-len, --partition-size) reaches
+    the reference arm as it reaches the library arm: the same configuration
+    dict, built from the same overrides."""
+    out = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+         "long_v2_bf16", "--num-seqs", "2", "--seq-len", "700", "--partition-size", "256",
+         "--steps", "2", "--warmup", "1", "--reference-budget", "1"],
+        capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    over = bench.workload_overrides("long_v2_bf16", 2, 700, 256)
+    assert over["seq_lens"] == [700, 700] and over["partition_size"] == 256
+    inp = workloads.make_workload("long_v2_bf16", seed=0, **over)
+    assert inp["spec"].partition_size == 256 and inp["seq_lens_list"] == [700, 700]
+    assert line["config"] == bench.workload_config(inp)
+    assert line["config"]["num_seqs"] == 2 and line["config"]["total_tokens"] == 1400
