@@ -204,9 +204,11 @@ __global__ void __launch_bounds__(WARPS * 32, (resident_ctas<KV, D, WARPS>()))
   // Split-KV over an fp8 cache: most partition slots of a sequence are empty
   // (it fills num_kv_splits of them), and an empty slot's CTA still holds a
   // residency slot while it reads the length and split count, which the
-  // latency-bound fp8 kernel feels.  Its two-warp instances therefore run up
-  // to two partitions per CTA (slots x and x + gridDim.x, grid x about half
-  // of max_parts), the second one's emptiness known without a further launch.
+  // latency-bound fp8 kernel feels.  Its two-warp instances therefore can run
+  // two partitions per CTA (slots x and x + gridDim.x, grid x about half of
+  // max_parts; p.fold, which the launcher sets for batches whose (sequence,
+  // kv head) pairs fill the GPU twice), the second one's emptiness known
+  // without a further launch.
   constexpr bool kTwoUnits = kFp8 && WARPS == 2;
   int unit_r = 0;
   {
