@@ -378,6 +378,41 @@ def test_copy_wait_timeout_is_reported_and_the_context_survives():
         assert_attention_close(out, _oracle_v1(inp), DT[dtype], f"after timeout {dtype}")
 
 
+def test_fp8_split_fold_stops_after_a_copy_timeout():
+    """Two partitions per CTA (fp8 cache, split-KV, halved grid forced): when
+    the first partition's copy waits run out (test hook, 20 ms limit) the
+    CTA reports PKV_ERRF_TIMEOUT and does not start its second partition on
+    the ring whose barriers still expect bytes; the next launches in the same
+    context are correct."""
+    lens = [700, 900]
+    inp = _inputs("bf16", 128, 16, 4, 1, lens, seed=51, kv_cache_dtype="fp8_e4m3", k_scale=0.5,
+                  v_scale=2.0)
+    g = on_device(inp)
+    splits = torch.full((len(lens),), 4, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.set_attention_warps(2)  # the fold exists on two-warp CTAs; small batches pick four
+    pkv.set_split_fold(2)
+    try:
+        pkv.set_wait_limit_ns(20_000_000)
+        pkv._test_set_unarrived_bytes(16)
+        try:
+            run_v2(g, 4, splits=splits, err=err)
+            torch.cuda.synchronize()
+        finally:
+            pkv._test_set_unarrived_bytes(0)
+            pkv.set_wait_limit_ns(0)
+        assert int(err.item()) & pkv.PKV_ERRF_TIMEOUT
+        err.zero_()
+        _, _, _, out = run_v2(g, 4, splits=splits, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+    finally:
+        pkv.set_split_fold(1)
+        pkv.set_attention_warps(0)
+    assert_attention_close(out, _oracle_v1(inp, **oracle_kwargs(inp)), torch.bfloat16,
+                           "after a timeout, two partitions per CTA")
+
+
 @pytest.mark.parametrize("dtype,kv,alibi", [("f32", "auto", False), ("bf16", "auto", True),
                                              ("f16", "fp8_e4m3", False), ("bf16", "fp8_e5m2", True)])
 def test_column_pair_and_full_forms_agree(dtype, kv, alibi):
@@ -462,6 +497,7 @@ def test_split_fold_is_bitwise_identical(dtype, kv, D, bs, H, Hk, maxP):
     s[2] = maxP  # as many splits as slots on 17 tokens: some of them empty
     s[4] = maxP - 1 if maxP > 1 else 1
     splits = s.to("cuda")
+    pkv.set_attention_warps(2)  # the fold exists on two-warp CTAs; small batches pick four
     try:
         pkv.set_split_fold(0)
         full = run_v2(g, maxP, splits=splits)
@@ -469,6 +505,7 @@ def test_split_fold_is_bitwise_identical(dtype, kv, D, bs, H, Hk, maxP):
         folded = run_v2(g, maxP, splits=splits)
     finally:
         pkv.set_split_fold(1)
+        pkv.set_attention_warps(0)
     for a, b, what in zip(full, folded, ("tmp_out", "exp_sums", "max_logits", "output")):
         assert _same(a, b), f"{what} differs between one and two partitions per CTA"
     tmp, es, ml, _ = folded
