@@ -477,7 +477,7 @@ def _same(a, b):
 @pytest.mark.parametrize("dtype,kv,D,bs,H,Hk,maxP", [
     ("f16", "fp8_e4m3", 128, 16, 32, 8, 16), ("bf16", "fp8_e4m3", 128, 16, 64, 8, 16),
     ("bf16", "fp8_e5m2", 64, 8, 16, 4, 9), ("f16", "fp8_e4m3", 256, 16, 72, 4, 5),
-    ("bf16", "fp8_e4m3", 128, 16, 8, 8, 2)])
+    ("bf16", "fp8_e4m3", 128, 16, 8, 8, 2), ("bf16", "fp8_e4m3", 128, 16, 32, 8, 40)])
 def test_split_fold_is_bitwise_identical(dtype, kv, D, bs, H, Hk, maxP):
     """Split-KV over an fp8 cache with half the partition slots (a CTA runs
     partitions x and x + slots of its sequence) gives bit-identical partials,
