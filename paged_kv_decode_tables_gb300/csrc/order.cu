@@ -41,13 +41,27 @@ __global__ void __launch_bounds__(kOrderThreads)
   const int ml = max_len;
   for (int i = tid; i < n; i += kOrderThreads) atomicAdd(&count[bucket_of(seq_lens[i], ml)], 1u);
   __syncthreads();
-  if (tid == 0) {
-    unsigned run = 0;
-    for (int b = 0; b < kBuckets; ++b) {
-      const unsigned c = count[b];
-      count[b] = run;  // first position of bucket b
-      run += c;
+  // Exclusive prefix sum of the bucket counts: one bucket per thread of the
+  // first kBuckets threads, an inclusive scan within each warp by shuffles,
+  // then the warps' totals added in.
+  __shared__ unsigned warp_total[kBuckets / 32];
+  const int lane = tid & 31, w = tid >> 5;
+  unsigned c = 0, incl = 0;
+  if (tid < kBuckets) {
+    c = count[tid];
+    incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
+    if (lane == 31) warp_total[w] = incl;
+  }
+  __syncthreads();
+  if (tid < kBuckets) {
+    unsigned base = 0;
+    for (int k = 0; k < w; ++k) base += warp_total[k];
+    count[tid] = base + incl - c;  // first position of bucket tid
   }
   __syncthreads();
   for (int i = tid; i < n; i += kOrderThreads) {
