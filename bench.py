@@ -210,7 +210,7 @@ class DecodeStep:
     straight through the C ABI with argument structs prepared once."""
 
     def __init__(self, name: str, seed: int, device, num_seqs=None, fused_metadata=True,
-                 lpt=False, seq_len=None, partition_size=None):
+                 lpt=True, seq_len=None, partition_size=None):
         import ctypes
 
         import paged_kv_decode_tables_gb300 as pkv
@@ -271,7 +271,11 @@ class DecodeStep:
                                   "v2_splits": 3 if fused_metadata else 4}[self.mode]
         # Single pass, longest sequence first: each step orders the batch on
         # the device (pkv_order_by_length) and the decode launches in that order.
-        self.lpt = lpt and self.mode == "v1"
+        # Only a batch of several waves has a tail worth shortening: at least
+        # 4 (sequence, kv head) units per SM.
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count if dev.type == "cuda" else 1
+        units = B * Hk * -(-(H // Hk) // 8)
+        self.lpt = lpt and self.mode == "v1" and units >= 4 * sms
         if self.lpt:
             self.order = torch.empty(B, dtype=torch.int32, device=dev)
             self.args.seq_order = self.order.data_ptr()
@@ -771,7 +775,8 @@ def dtype_label(spec):
 def companion_record(name, args, peak, peak_kind, want_one_core):
     """Time one companion workload (same steps and warm-up as the headline)
     and, for the small and mid-size configurations, its oracle on one core."""
-    step = DecodeStep(name, seed=0, device="cuda")
+    step = DecodeStep(name, seed=0, device="cuda",
+                      lpt=args.launch_order == "longest-first")
     K = args.steps
     clocks = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
     per_step, span, graphed, clk = time_steps(step, K, args.warmup, args.graph, clocks=clocks)
@@ -788,6 +793,8 @@ def companion_record(name, args, peak, peak_kind, want_one_core):
         "kernel_us": kernel_us,
         "gpu_launches": K * step.launches_per_step,
         "launch": "CUDA graph replay of the step" if graphed else "stream launches",
+        "launch_order": ("longest first (pkv_order_by_length in the step)" if step.lpt
+                         else "sequence order"),
         "clocks": clk,
     }
     if want_one_core:
@@ -817,7 +824,8 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     step = DecodeStep(args.workload, seed=rank, device="cuda", num_seqs=args.num_seqs,
-                      fused_metadata=args.metadata == "fused", lpt=args.lpt,
+                      fused_metadata=args.metadata == "fused",
+                      lpt=args.launch_order == "longest-first",
                       seq_len=args.seq_len, partition_size=args.partition_size)
     if args.warps:
         step.pkv.set_attention_warps(args.warps)
@@ -1127,8 +1135,10 @@ def main(argv=None):
                     help="kernel for fp8 caches of head size 128 / block size 16")
     ap.add_argument("--metadata", choices=["fused", "separate"], default="fused",
                     help="ragged step: metadata in one launch or the two separate kernels")
-    ap.add_argument("--lpt", action="store_true",
-                    help="single pass: order the batch longest first on the device each step")
+    ap.add_argument("--launch-order", choices=["longest-first", "sequence"],
+                    default="longest-first",
+                    help="single pass: order the batch longest first on the device each step "
+                         "(pkv_order_by_length, one launch in the step) or keep sequence order")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time stream launches instead of CUDA-graph replays of the step")
     ap.add_argument("--no-clocks", action="store_true")
