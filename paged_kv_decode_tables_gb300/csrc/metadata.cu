@@ -82,6 +82,30 @@ __device__ __forceinline__ void copy_row_segment(int32_t *__restrict__ out, int6
   }
 }
 
+// log2(x) correctly rounded to float32 through the float64 log2; not
+// inlined, so that it runs only when called (the compiler would otherwise be
+// free to evaluate it ahead of the branch that needs it).
+__device__ __noinline__ float log2_rounded_f32(float x) {
+  return __double2float_rn(log2(double(x)));
+}
+
+// trunc(core_count * max(r, 1)) in float32, where r is log2(ext_len)
+// correctly rounded to float32.  Only that integer matters, so the float64
+// log2 (slow on this GPU) is needed only near a truncation boundary:
+// log2f is within 1 ulp of log2 (its documented bound), so r is one of
+// log2f(ext_len) and its two float neighbours; when all three give the same
+// integer, that integer is the answer; otherwise r is computed from the
+// float64 log2 rounded once.
+__device__ __forceinline__ int64_t ext_core_count(float ext_len, float cores) {
+  auto ext_of = [cores](float r) -> int64_t {
+    return __float2int_rz(__fmul_rn(cores, fmaxf(r, 1.0f)));
+  };
+  const float y = log2f(ext_len);
+  const int64_t e = ext_of(y);
+  if (ext_of(nextafterf(y, -INFINITY)) == e && ext_of(nextafterf(y, INFINITY)) == e) return e;
+  return ext_of(log2_rounded_f32(ext_len));
+}
+
 // The split-count heuristic on one CTA of THREADS threads.
 template <int THREADS>
 __device__ __forceinline__ void split_counts(int32_t *__restrict__ out,
@@ -120,9 +144,7 @@ __device__ __forceinline__ void split_counts(int32_t *__restrict__ out,
     // The one float32 step: log2(max_len / 64) rounded to float32, times the
     // core count in float32, truncated toward zero.
     const float ext_len = __fdiv_rn(__int2float_rn(mx), 64.0f);
-    const float lg = __double2float_rn(log2(double(ext_len)));
-    const float prod = __fmul_rn(__int2float_rn(core_count), fmaxf(lg, 1.0f));
-    const int64_t ext = __float2int_rz(prod);
+    const int64_t ext = ext_core_count(ext_len, __int2float_rn(core_count));
     const int kv_group = num_head / num_kv_head;
     int64_t token_grid;
     if (kv_group == 1) {

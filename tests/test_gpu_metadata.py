@@ -3,6 +3,7 @@
 (hand-worked cases and an exhaustive sweep of the float32 step)."""
 import os
 
+import numpy as np
 import pytest
 import torch
 
@@ -93,6 +94,41 @@ def test_num_kv_splits_random_batches():
         ng = 1 + trial % 3
         got = _gpu_splits(lens, ng, nh, nkv, mx, 148).cpu().tolist()
         assert got == oracle.num_kv_splits(lens, ng, nh, nkv, mx, 148), trial
+
+
+def test_num_kv_splits_float32_step_large_lengths():
+    """The float32 step on 20,000 seeded random max_seq_len in [2^18, 2^31)
+    and on every length whose float32 intermediate the oracle puts within
+    3e-4 of an integer in a further 200,000 draws (where a one-ulp error in
+    the log2 would move the truncation), with the same construction as the
+    exhaustive test below: token_grid = e and e - 1."""
+    gen = torch.Generator().manual_seed(61)
+    draws = torch.randint(1 << 18, (1 << 31) - 1, (220_000,), generator=gen).tolist()
+    lens = draws[:20_000]
+    for L in draws[20_000:]:
+        ext_len = np.float32(np.float32(L) / np.float32(64.0))
+        lg = np.float32(np.log2(np.float64(ext_len)))
+        prod = np.float32(np.float32(148.0) * max(lg, np.float32(1.0)))
+        if abs(float(prod) - round(float(prod))) < 3e-4:
+            lens.append(L)
+    N = len(lens)
+    assert N > 20_000
+    dl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    lib = pkv.lib()
+    out = torch.full((2 * N,), -1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    base_l, base_o = dl.data_ptr(), out.data_ptr()
+    want = []
+    for i, L in enumerate(lens):
+        e = oracle.ext_device_core_count(L, 148)
+        for j, tg in enumerate((e, max(e - 1, 1))):
+            st = lib.compute_num_kv_splits(base_o + 4 * (2 * i + j), base_l + 4 * i, 1, 1, tg, tg,
+                                           1 << 30, 148, stream)
+            assert st == 0
+            want.append(oracle.num_kv_splits([L], 1, tg, tg, 1 << 30, 148)[0])
+    got = out.cpu().tolist()
+    bad = [(lens[k // 2], got[k], want[k]) for k in range(2 * N) if got[k] != want[k]]
+    assert not bad, bad[:10]
 
 
 def test_num_kv_splits_float32_step_exhaustive():
