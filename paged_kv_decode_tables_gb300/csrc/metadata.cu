@@ -91,7 +91,8 @@ __device__ __noinline__ float log2_rounded_f32(float x) {
 
 // trunc(core_count * max(r, 1)) in float32, where r is log2(ext_len)
 // correctly rounded to float32.  Only that integer matters, so the float64
-// log2 (slow on this GPU) is needed only near a truncation boundary:
+// log2 (float64 runs at a small fraction of the float32 rate on GB300) is
+// needed only near a truncation boundary:
 // log2f is within 1 ulp of log2 (its documented bound), so r is one of
 // log2f(ext_len) and its two float neighbours; when all three give the same
 // integer, that integer is the answer; otherwise r is computed from the
